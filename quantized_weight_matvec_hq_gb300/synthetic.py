@@ -1,0 +1,79 @@
+"""Seeded synthetic inputs for the quantized-weight matvec.
+
+This module only draws random numbers: it holds none of the method's
+arithmetic (no quantization, no dequantization, no dot products), so that the
+CPU oracle and the CUDA path can both be fed from it without sharing any step
+of the computation.  It imports neither the oracle nor the CUDA library.
+
+The recipe follows the workloads on the pages:
+
+* weights W ~ N(0, 0.02) fp32, quantized afterwards by each side's own
+  quantizer;
+* activations x ~ N(0, 1) fp32, ``n_vec`` vectors of one length (n_vec 1..8:
+  batch-1 decode up to the speculative-verify widths q in [1, 8] of
+  "DeepSeek-V4 on Hanzo Engine", section "A Fused Attention Kernel for
+  512-Wide Latent Heads");
+* MoE routing: every token picks ``n_active`` distinct experts uniformly at
+  random (a draw without replacement), slot order as drawn.
+
+Generator: NumPy ``Generator(PCG64(seed))``.  The default seed of workload i is
+``SEED_BASE + i``.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+SEED_BASE = 20261202
+
+# Decode shapes (rows = output features, cols = input features).
+QWEN3_0_6B_LAYER = (
+    ("q", 2048, 1024), ("k", 1024, 1024), ("v", 1024, 1024), ("o", 1024, 2048),
+    ("gate", 3072, 1024), ("up", 3072, 1024), ("down", 1024, 3072),
+)
+QWEN3_0_6B_LAYERS = 28
+QWEN3_0_6B_LM_HEAD = ("lm_head", 151936, 1024)
+
+DENSE_8B_LAYER = (
+    ("q", 4096, 4096), ("k", 1024, 4096), ("v", 1024, 4096), ("o", 4096, 4096),
+    ("gate", 14336, 4096), ("up", 14336, 4096), ("down", 4096, 14336),
+)
+DENSE_8B_LAYERS = 32
+DENSE_8B_LM_HEAD = ("lm_head", 128256, 4096)
+
+MOE_N_EXPERTS = 128
+MOE_N_ACTIVE = 8
+MOE_HIDDEN = 2048
+MOE_FFN = 768
+
+INT8_SHAPES = ((1024, 3072), (3072, 1024))
+
+
+def rng(seed: int) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def weights(g: np.random.Generator, rows: int, cols: int, std: float = 0.02) -> np.ndarray:
+    """fp32 [rows][cols] ~ N(0, std)."""
+    return g.standard_normal((rows, cols), dtype=np.float32) * np.float32(std)
+
+
+def activations(g: np.random.Generator, n_vec: int, cols: int) -> np.ndarray:
+    """fp32 [n_vec][cols] ~ N(0, 1)."""
+    return g.standard_normal((n_vec, cols), dtype=np.float32)
+
+
+def expert_ids(g: np.random.Generator, n_vec: int, n_active: int, n_experts: int) -> np.ndarray:
+    """int32 [n_vec][n_active]: distinct experts per token, uniformly at random."""
+    out = np.empty((n_vec, n_active), dtype=np.int32)
+    for t in range(n_vec):
+        out[t] = g.permutation(n_experts)[:n_active]
+    return out
+
+
+def decode_token_shapes(model: str):
+    """The (name, rows, cols) list of one decode token's matvecs, lm_head last."""
+    if model == "qwen3-0.6b":
+        return [s for _ in range(QWEN3_0_6B_LAYERS) for s in QWEN3_0_6B_LAYER] + [QWEN3_0_6B_LM_HEAD]
+    if model == "8b-dense":
+        return [s for _ in range(DENSE_8B_LAYERS) for s in DENSE_8B_LAYER] + [DENSE_8B_LM_HEAD]
+    raise ValueError(model)

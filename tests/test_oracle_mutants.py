@@ -1,0 +1,142 @@
+"""Planted mistakes: each test copies the C oracle to a temporary directory,
+plants one plausible bug by a textual edit (a dropped term, a wrong sign or
+index, a swapped nibble, a transposed operand, a wrong rounding rule), builds
+it with gcc and runs the same pins the real oracle passes.  At least one pin
+must catch every mutant.  Nothing here touches the GPU or the product.
+"""
+import ctypes
+import json
+import os
+import subprocess
+
+import numpy as np
+import pytest
+
+import oracle
+from oracle import oracle_np
+from quantized_weight_matvec_hq_gb300 import synthetic
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "hq_oracle.c")
+
+MUTANTS = {
+    "nibble_order_swapped": ("int lo = blk[2 + j] & 0x0f;\n                int hi = blk[2 + j] >> 4;",
+                             "int hi = blk[2 + j] & 0x0f;\n                int lo = blk[2 + j] >> 4;"),
+    "matvec_nibble_order_swapped": ("(j < 16 ? (blk[2 + j] & 0x0f) : (blk[2 + j - 16] >> 4))",
+                                    "(j < 16 ? (blk[2 + j] >> 4) : (blk[2 + j - 16] & 0x0f))"),
+    "q8_unsigned_quants": ("if (fmt == 8) q = (int8_t)blk[2 + j];", "if (fmt == 8) q = (uint8_t)blk[2 + j];"),
+    "dropped_last_element": ("for (int j = 0; j < HQO_QK; ++j) {\n                    int q;",
+                             "for (int j = 0; j < HQO_QK - 1; ++j) {\n                    int q;"),
+    "q4_offset_7": ("- 8;\n                    double w = d * (double)q;", "- 7;\n                    double w = d * (double)q;"),
+    "transposed_x": ("x[(int64_t)v * cols + b * HQO_QK + j]", "x[(b * HQO_QK + j) * n_vec + v]"),
+    "scale_wrong_byte_order": ("static uint16_t load_u16le(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }",
+                               "static uint16_t load_u16le(const uint8_t *p) { return (uint16_t)(p[1] | (p[0] << 8)); }"),
+    "srdhm_nudge_sign": ("int64_t nudge = ab >= 0 ? ((int64_t)1 << 30) : (1 - ((int64_t)1 << 30));",
+                         "int64_t nudge = ((int64_t)1 << 30);"),
+    "rdivbypot_no_negative_adjust": ("int64_t thr = (mask >> 1) + (x < 0 ? 1 : 0);", "int64_t thr = (mask >> 1);"),
+    "requant_order_swapped": ("int32_t r = hqo_rdivbypot(hqo_srdhm(acc, mult), shift);",
+                              "int32_t r = hqo_srdhm(hqo_rdivbypot(acc, shift), mult);"),
+    "half_ties_away": ("if (rem > 0.5 || (rem == 0.5 && (ki & 1u))) ki += 1;", "if (rem >= 0.5) ki += 1;"),
+    "q8_scale_254": ("float d = amax / 127.0f;\n            uint16_t dh", "float d = amax / 254.0f;\n            uint16_t dh"),
+    "q4_scale_positive": ("float d = m / -8.0f;", "float d = m / 8.0f;"),
+    "q4_round_down": ("float t = w[j] / d + 8.5f;", "float t = w[j] / d + 8.0f;"),
+}
+
+
+def _build_mutant(tmp_path, name):
+    src = open(SRC).read()
+    old, new = MUTANTS[name]
+    assert src.count(old) == 1, f"mutation site for {name} not found exactly once"
+    p = tmp_path / f"{name}.c"
+    p.write_text(src.replace(old, new))
+    so = tmp_path / f"{name}.so"
+    subprocess.run(["gcc", "-O1", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off",
+                    "-o", str(so), str(p), "-lm"], check=True)
+    L = ctypes.CDLL(str(so))
+    vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    for fn in ("hqo_quantize_q8_0", "hqo_quantize_q4_0"):
+        getattr(L, fn).argtypes = [vp, i64, i64, vp]
+    for fn in ("hqo_dequant_q8_0", "hqo_dequant_q4_0"):
+        getattr(L, fn).argtypes = [vp, i64, i64, vp]
+    for fn in ("hqo_matvec_q8_0", "hqo_matvec_q4_0"):
+        getattr(L, fn).argtypes = [vp, vp, i64, i64, ci, vp, vp]
+    L.hqo_srdhm.argtypes = [ctypes.c_int32, ctypes.c_int32]
+    L.hqo_srdhm.restype = ctypes.c_int32
+    L.hqo_rdivbypot.argtypes = [ctypes.c_int32, ci]
+    L.hqo_rdivbypot.restype = ctypes.c_int32
+    L.hqo_requant.argtypes = [ctypes.c_int32] * 3
+    L.hqo_requant.restype = ctypes.c_int8
+    L.hqo_float_to_half_rne.argtypes = [ctypes.c_float]
+    L.hqo_float_to_half_rne.restype = ctypes.c_uint16
+    return L
+
+
+def _pins_fail(L, golden_dir):
+    """Run the oracle's pins against library L; return the names of those that fail."""
+    failed = []
+    ptr = lambda a: a.ctypes.data
+    # golden blocks
+    gold = json.load(open(os.path.join(golden_dir, "blocks.json")))["blocks"]
+    from test_oracle_blocks import _weights
+    for b in gold:
+        w = _weights(b["name"])
+        out = np.empty(34 if b["format"] == "q8_0" else 18, np.uint8)
+        fn = L.hqo_quantize_q8_0 if b["format"] == "q8_0" else L.hqo_quantize_q4_0
+        fn(ptr(w), 1, 32, ptr(out))
+        if out.tobytes() != bytes.fromhex(b["bytes_hex"]):
+            failed.append("golden:" + b["name"])
+    # the independent vectorised quantizers, byte for byte
+    g = synthetic.rng(78)
+    W = synthetic.weights(g, 16, 128)
+    for fmt, bpb in (("q8_0", 34), ("q4_0", 18)):
+        out = np.empty((16, 4 * bpb), np.uint8)
+        (L.hqo_quantize_q8_0 if fmt == "q8_0" else L.hqo_quantize_q4_0)(ptr(W), 16, 128, ptr(out))
+        ref = oracle_np.quantize_q8_0(W) if fmt == "q8_0" else oracle_np.quantize_q4_0(W)
+        if not np.array_equal(out, ref):
+            failed.append("quantizer:" + fmt)
+    # brute force matvec and dequant on tiny shapes
+    for fmt in ("q8_0", "q4_0"):
+        g = synthetic.rng(77)
+        rows, cols, n_vec = 5, 96, 3
+        W = synthetic.weights(g, rows, cols)
+        blocks = oracle.quantize_q8_0(W) if fmt == "q8_0" else oracle.quantize_q4_0(W)
+        x = synthetic.activations(g, n_vec, cols)
+        y = np.empty((n_vec, rows)); T = np.empty((n_vec, rows))
+        (L.hqo_matvec_q8_0 if fmt == "q8_0" else L.hqo_matvec_q4_0)(
+            ptr(blocks), ptr(x), rows, cols, n_vec, ptr(y), ptr(T))
+        y_ref, _ = oracle_np.matvec(fmt, blocks, x, rows, cols)
+        if not np.allclose(y, y_ref, rtol=1e-12, atol=1e-12):
+            failed.append("brute:" + fmt)
+        Wd = np.empty((rows, cols))
+        (L.hqo_dequant_q8_0 if fmt == "q8_0" else L.hqo_dequant_q4_0)(ptr(blocks), rows, cols, ptr(Wd))
+        ref = oracle_np.dequant_q8_0(blocks, rows, cols) if fmt == "q8_0" else oracle_np.dequant_q4_0(blocks, rows, cols)
+        if not np.array_equal(Wd, ref):
+            failed.append("dequant:" + fmt)
+    # integer rules
+    w = json.load(open(os.path.join(golden_dir, "gemmlowp_worked.json")))
+    if any(L.hqo_srdhm(c["a"], c["b"]) != c["out"] for c in w["srdhm"]):
+        failed.append("srdhm")
+    if any(L.hqo_rdivbypot(c["x"], c["e"]) != c["out"] for c in w["rdivbypot"]):
+        failed.append("rdivbypot")
+    if any(L.hqo_requant(c["acc"], c["mult"], c["shift"]) != c["out"] for c in w["requant"]):
+        failed.append("requant")
+    # half conversion ties
+    h = np.arange(0, 0x7BFF, dtype=np.uint16)
+    mids = ((h.view(np.float16).astype(np.float64) + (h + 1).view(np.float16).astype(np.float64)) / 2)
+    mids = mids[mids == mids.astype(np.float32).astype(np.float64)].astype(np.float32)[::37]
+    ref = mids.astype(np.float16).view(np.uint16)
+    if any(L.hqo_float_to_half_rne(float(v)) != r for v, r in zip(mids, ref)):
+        failed.append("half")
+    return failed
+
+
+def test_unmutated_oracle_passes_all_pins(tmp_path, golden_dir):
+    MUTANTS["identity"] = ("int hqo_version(void) { return 1; }", "int hqo_version(void) { return 1; }")
+    try:
+        assert _pins_fail(_build_mutant(tmp_path, "identity"), golden_dir) == []
+    finally:
+        del MUTANTS["identity"]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(tmp_path, golden_dir, name):
+    assert _pins_fail(_build_mutant(tmp_path, name), golden_dir), f"mutant {name} passed every pin"
