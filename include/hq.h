@@ -1,0 +1,205 @@
+/*
+ * hq.h -- C ABI of the GB300 (sm_103a) quantized-weight matvec library (libhq.so).
+ *
+ * The library computes the bandwidth-bound decode product y = W_deq . x over
+ * block-quantized weights, for 1..8 activation vectors in one pass, so that
+ * every weight byte is streamed from HBM once per call.
+ *
+ * Sources (page title, section):
+ *   - "One Native Stack for Private, Continuously-Learning AI", section "The
+ *     Unified Quant Core": one quant-agnostic decode matvec over the ggml
+ *     block formats Q8_0 (symmetric, 34 B per 32 weights) and Q4_0
+ *     (symmetric, 18 B per 32 weights); the same core evaluates every routed
+ *     MoE expert.  Section "The Central Efficiency Thesis", Lemma "QLoRA over
+ *     the unified core is exact": y_i = sum_j What_ij x_j, What the CPU
+ *     dequantization of the stored bytes, accumulated in f32.
+ *   - "Economical Serving and the hanzo.ai Platform", subsection "The Roofline
+ *     that Sets the Price": decode time per token is W/B (weight bytes over
+ *     bandwidth); subsection "One Quant-Agnostic Core": per-format block
+ *     decoder + traits record, reused by decode and MoE.
+ *   - "Blue -- porting zen-nano (Qwen3-0.6B) to deterministic on-chain
+ *     inference", section "Quantization recipe (validated)": per-output-channel
+ *     symmetric int8 weights and gemmlowp requant
+ *     (SaturatingRoundingDoublingHighMul, then RoundingDivideByPOT) to int8.
+ *   - "DeepSeek-V4 on Hanzo Engine", section "A Fused Attention Kernel for
+ *     512-Wide Latent Heads": speculative-verify widths q in [1, 8], hence
+ *     n_vec in [1, 8].
+ *
+ * Conventions shared by every entry point
+ *   - Pointers named W, x, y, ids, mult, shift, acc, out, scale are DEVICE
+ *     pointers owned by the caller (cudaMalloc / PyTorch).  The library never
+ *     allocates, frees or retains them, and keeps no state between calls other
+ *     than a thread-local error string and a device fault word (below).
+ *   - Every call is asynchronous and stream-ordered on `stream` (a
+ *     cudaStream_t; NULL is the legacy default stream).  Arguments are
+ *     validated on the host before any launch; a non-OK status means nothing
+ *     was launched (except HQ_ERR_LAUNCH, which reports the launch failure).
+ *     A fault inside a kernel surfaces at the caller's next synchronization.
+ *   - Row-major layouts.  Quantized rows are packed blocks with no padding:
+ *     row i of a Q8_0 matrix is bytes [i*cols/32*34, (i+1)*cols/32*34).
+ *   - Block layouts (little-endian): Q8_0 = { uint16 fp16 d; int8 q[32] },
+ *     w_j = d*q_j.  Q4_0 = { uint16 fp16 d; uint8 qs[16] }, element j (0..15)
+ *     is the low nibble of qs[j] and element j+16 the high nibble,
+ *     w = d*(n - 8).
+ *   - Float paths accumulate in fp32 and are deterministic run to run (fixed
+ *     reduction order, no float atomics).  They match the f64 definition
+ *     within |y - y_ref| <= 1e-3 * sum_j |w_deq x_j| + 1e-5 per output.
+ *     The int8 path is bit-exact.
+ *   - Shapes: rows >= 1, cols >= 32, cols % 32 == 0 (int8: cols >= 4 and
+ *     cols % 4 == 0), 1 <= n_vec <= 8.  W and x must be 16-byte aligned.
+ *     When cols % 256 == 0 (every decode shape) the TMA-staged kernel runs;
+ *     other legal shapes run a plain-load kernel that gives the same results
+ *     to the same tolerance.  There is no CPU fallback.
+ */
+#ifndef HQ_H_
+#define HQ_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *hq_stream_t;   /* identical to cudaStream_t */
+
+typedef enum {
+    HQ_OK = 0,
+    HQ_ERR_NULL = -1,         /* a required pointer is NULL                        */
+    HQ_ERR_SHAPE = -2,        /* rows/cols/n_experts/n_active out of range         */
+    HQ_ERR_ALIGN = -3,        /* W or x not 16-byte aligned (y: 4-byte)            */
+    HQ_ERR_NVEC = -4,         /* n_vec not in [1, 8]                               */
+    HQ_ERR_LAUNCH = -5,       /* the CUDA launch failed (see hq_last_error)        */
+    HQ_ERR_UNSUPPORTED = -6,  /* no sm_100-family GPU, or a value not representable */
+    HQ_ERR_DEVICE = -7        /* a kernel reported a fault word (hq_device_fault)  */
+} hq_status;
+
+/* Library version (major*10000 + minor*100 + patch). */
+int hq_version(void);
+
+/* Message for the last non-OK status returned on this host thread ("" if none). */
+const char *hq_last_error(void);
+
+/*
+ * hq_matvec_q8_0 -- y[v][i] = sum_j w_deq[i][j] * x[v][j] for v < n_vec, i < rows.
+ *   W  : Q8_0 blocks, rows x (cols/32) x 34 bytes, 16-byte aligned.
+ *   x  : fp32 [n_vec][cols], 16-byte aligned.
+ *   y  : fp32 [n_vec][rows], overwritten (not accumulated).
+ * Source: "One Native Stack ...", section "The Unified Quant Core" (Q8_0,
+ * 34 B/32) and the Lemma of section "The Central Efficiency Thesis".
+ */
+hq_status hq_matvec_q8_0(const void *W, const float *x, float *y,
+                         int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
+
+/*
+ * hq_matvec_q4_0 -- as hq_matvec_q8_0 for Q4_0 blocks (rows x cols/32 x 18 B):
+ * w = d * (n - 8), nibble order as in the conventions above.
+ * Source: "One Native Stack ...", section "The Unified Quant Core" (Q4_0, 18 B/32).
+ */
+hq_status hq_matvec_q4_0(const void *W, const float *x, float *y,
+                         int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
+
+/*
+ * hq_matvec_i8_requant -- per-output-channel int8 GEMV with gemmlowp requant:
+ *   acc = sum_j W[o][j] * x[v][j]  (int32; the caller keeps it in range:
+ *         |W|, |x| <= 127 and cols < 133,000 always fit),
+ *   y[v][o] = clamp(RDivByPOT(SRDHM(acc, mult[o]), shift[o]), -128, 127).
+ *   W     : int8 [rows][cols], 16-byte aligned.   x : int8 [n_vec][cols], 16-byte aligned.
+ *   mult  : int32 [rows] (any value).             shift : int32 [rows], each in [0, 31].
+ *   y     : int8 [n_vec][rows].
+ * SRDHM(a,b) is the high word of 2ab rounded to nearest (ties toward +inf),
+ * saturating only at a = b = INT32_MIN; RDivByPOT(x,e) is x/2^e rounded to
+ * nearest with ties away from zero.  Bit-exact.  A shift outside [0,31] is a
+ * precondition violation (the kernel clamps it to that range).
+ * Source: "Blue -- porting zen-nano ...", section "Quantization recipe
+ * (validated)" and section "Gaps vs the current toy engine", item 3.
+ */
+hq_status hq_matvec_i8_requant(const int8_t *W, const int8_t *x,
+                               const int32_t *mult, const int32_t *shift, int8_t *y,
+                               int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
+
+/*
+ * hq_moe_matvec_q8_0 -- expert-indexed, grouped Q8_0 matvec for MoE decode.
+ *   W_bank     : n_experts Q8_0 matrices of rows x cols, back to back
+ *                (expert e starts at byte e*rows*cols/32*34), 16-byte aligned.
+ *   expert_ids : int32 [n_vec][n_active], each in [0, n_experts).
+ *   x          : fp32 [n_vec][cols] when x_per_slot == 0 (all slots of token t
+ *                share x[t], as for gate/up), or [n_vec][n_active][cols] when
+ *                x_per_slot == 1 (one input per slot, as for down).
+ *   y          : fp32 [n_vec][n_active][rows]; y[t][k] = W_bank[ids[t][k]] . x(t,k).
+ * Slots that pick the same expert are grouped so that each chosen expert's
+ * bytes are streamed once per call.  No router weighting is applied.  An id
+ * outside [0, n_experts) is a precondition violation: its outputs are set to
+ * NaN and the device fault word gets HQ_FAULT_EXPERT_ID; nothing traps.
+ * Source: "One Native Stack ...", section "The Unified Quant Core" (the MoE
+ * path dispatches each routed expert through the same core); "Economical
+ * Serving ...", subsection "The Roofline that Sets the Price" (MoE reads
+ * only its active parameters).
+ */
+hq_status hq_moe_matvec_q8_0(const void *W_bank, const int32_t *expert_ids,
+                             const float *x, int x_per_slot, float *y,
+                             int64_t n_experts, int n_active, int64_t rows, int64_t cols,
+                             int n_vec, hq_stream_t stream);
+
+/*
+ * Quantizers (the one-off data-preparation step, on the GPU).
+ * hq_quantize_q8_0: W fp32 [rows][cols] (device) -> out Q8_0 blocks (device):
+ *   d = max|w|/127 in fp32, stored fp16 (round to nearest even);
+ *   q = round(w/d) (fp32 division, half away from zero), clamped to [-127,127];
+ *   an all-zero block stores d = 0 and q = 0.
+ * hq_quantize_q4_0: d = m/-8 with m the block's largest-|w| element (first
+ *   on ties, sign kept), stored fp16; n = min(15, floor(w/d + 8.5)) (fp32);
+ *   an all-zero block stores d = -0 and n = 8.
+ * hq_quantize_i8_rows: scale[o] = max|W[o,:]|/127 (fp32),
+ *   Wq = round(W/scale) clamped to [-127,127]; with rows = 1 this is the
+ *   static per-tensor activation quantizer.
+ * Requires rows >= 1 and cols % 32 == 0 (i8: cols >= 1); W 4-byte aligned.
+ * Source: "One Native Stack ...", section "The Unified Quant Core" (formats
+ * taken verbatim from ggml); "Blue -- porting zen-nano ...", section
+ * "Quantization recipe (validated)".
+ */
+hq_status hq_quantize_q8_0(const float *W, void *out, int64_t rows, int64_t cols,
+                           hq_stream_t stream);
+hq_status hq_quantize_q4_0(const float *W, void *out, int64_t rows, int64_t cols,
+                           hq_stream_t stream);
+hq_status hq_quantize_i8_rows(const float *W, int8_t *Wq, float *scale,
+                              int64_t rows, int64_t cols, hq_stream_t stream);
+
+/*
+ * hq_requant_params -- HOST function: real multipliers M[i] in (0, 1) to
+ * (mult, shift) with M ~= mult * 2^-31 * 2^-shift: M = f * 2^-shift with
+ * f in [0.5, 1), mult = round(f * 2^31) (half away from zero; 2^31 becomes
+ * 2^30 with shift - 1).  M, mult, shift are HOST arrays of n elements.
+ * Returns HQ_ERR_UNSUPPORTED if some M is outside (0,1) or needs shift > 31.
+ * Source: "Blue -- porting zen-nano ...", section "Quantization recipe
+ * (validated)" (the requant multiplier s_a*s_w[o]/s_out as an integer pair).
+ */
+hq_status hq_requant_params(const double *M, int64_t n, int32_t *mult, int32_t *shift);
+
+/*
+ * hq_requant_i32_debug -- applies the device requant epilogue of
+ * hq_matvec_i8_requant to arbitrary int32 accumulators, so that values the
+ * GEMV cannot reach (INT32_MIN, INT32_MAX) are tested bit-exactly:
+ * y[i] = requant(acc[i], mult[i % rows], shift[i % rows]).  Device pointers;
+ * acc, y have n elements, mult, shift have rows elements.
+ * Source: as hq_matvec_i8_requant.
+ */
+hq_status hq_requant_i32_debug(const int32_t *acc, const int32_t *mult, const int32_t *shift,
+                               int8_t *y, int64_t n, int64_t rows, hq_stream_t stream);
+
+/*
+ * Device fault word.  Kernels never trap: a bounded wait that gives up (a
+ * TMA transfer that never completes) or an out-of-range expert id sets a bit
+ * in a per-device word and the kernel finishes without using the missing
+ * data.  hq_device_fault() synchronizes the current device, returns the word
+ * in *fault (0 = none) and clears it; it returns HQ_ERR_DEVICE if the word
+ * was non-zero.
+ */
+#define HQ_FAULT_WAIT_TIMEOUT 1u   /* an mbarrier wait exceeded its time limit */
+#define HQ_FAULT_EXPERT_ID    2u   /* an expert id outside [0, n_experts)      */
+hq_status hq_device_fault(uint32_t *fault);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HQ_H_ */

@@ -1,0 +1,217 @@
+// hq_api.cu -- the C ABI declared in include/hq.h: argument validation, error
+// reporting, per-device set-up, and dispatch to the kernels.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "hq_internal.h"
+
+namespace hq {
+
+// The fault word that kernels set instead of trapping (see hq.h).
+__device__ uint32_t g_fault_word;
+
+namespace {
+
+thread_local char t_error[512] = "";
+std::mutex g_mutex;
+constexpr int kMaxDevices = 64;
+DeviceInfo g_devices[kMaxDevices];
+void *g_encoder = nullptr;
+bool g_encoder_tried = false;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+hq_status set_error(hq_status st, const char *fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(t_error, sizeof(t_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+hq_status device_info(DeviceInfo **out) {
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return set_error(HQ_ERR_UNSUPPORTED, "no CUDA device: %s", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return set_error(HQ_ERR_UNSUPPORTED, "device index %d too large", dev);
+    DeviceInfo &d = g_devices[dev];
+    if (d.device == dev) { *out = &d; return HQ_OK; }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (d.device != dev) {
+        DeviceInfo n;
+        n.device = dev;
+        if (cudaDeviceGetAttribute(&n.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&n.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return set_error(HQ_ERR_UNSUPPORTED, "cudaDeviceGetAttribute failed");
+        if (n.cc_major != 10 || n.cc_minor != 3)
+            return set_error(HQ_ERR_UNSUPPORTED, "built for sm_103a; device %d is sm_%d%d", dev, n.cc_major, n.cc_minor);
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_fault_word);
+        if (e != cudaSuccess) return set_error(HQ_ERR_UNSUPPORTED, "fault word: %s", cudaGetErrorString(e));
+        n.fault = static_cast<uint32_t *>(p);
+        d = n;
+    }
+    *out = &d;
+    return HQ_OK;
+}
+
+void *tensor_map_encoder() {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_encoder_tried) {
+        g_encoder_tried = true;
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            g_encoder = fn;
+    }
+    return g_encoder;
+}
+
+}  // namespace hq
+
+using namespace hq;
+
+namespace {
+
+hq_status check_float_matvec(const void *W, const float *x, float *y, int64_t rows, int64_t cols, int n_vec) {
+    if (!W || !x || !y) return set_error(HQ_ERR_NULL, "W, x and y must be non-null");
+    if (n_vec < 1 || n_vec > 8) return set_error(HQ_ERR_NVEC, "n_vec %d not in [1,8]", n_vec);
+    if (rows < 1 || rows > 0x7fffffffLL || cols < 32 || cols % 32 != 0 || cols > (1LL << 31))
+        return set_error(HQ_ERR_SHAPE, "bad shape rows=%lld cols=%lld (need rows>=1, cols>=32, cols%%32==0)",
+                         (long long)rows, (long long)cols);
+    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(y, 4))
+        return set_error(HQ_ERR_ALIGN, "W and x must be 16-byte aligned, y 4-byte aligned");
+    return HQ_OK;
+}
+
+hq_status finish(hq_status st) {
+    if (st == HQ_OK) t_error[0] = '\0';
+    return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+int hq_version(void) { return 1 * 10000 + 0 * 100 + 0; }
+
+const char *hq_last_error(void) { return t_error; }
+
+hq_status hq_matvec_q8_0(const void *W, const float *x, float *y, int64_t rows, int64_t cols,
+                         int n_vec, hq_stream_t stream) {
+    hq_status st = check_float_matvec(W, x, y, rows, cols, n_vec);
+    if (st != HQ_OK) return st;
+    return finish(launch_matvec_float_q8_0(W, x, y, rows, cols, n_vec, (cudaStream_t)stream));
+}
+
+hq_status hq_matvec_q4_0(const void *W, const float *x, float *y, int64_t rows, int64_t cols,
+                         int n_vec, hq_stream_t stream) {
+    hq_status st = check_float_matvec(W, x, y, rows, cols, n_vec);
+    if (st != HQ_OK) return st;
+    return finish(launch_matvec_float_q4_0(W, x, y, rows, cols, n_vec, (cudaStream_t)stream));
+}
+
+hq_status hq_matvec_i8_requant(const int8_t *W, const int8_t *x, const int32_t *mult,
+                               const int32_t *shift, int8_t *y, int64_t rows, int64_t cols, int n_vec,
+                               hq_stream_t stream) {
+    if (!W || !x || !mult || !shift || !y) return set_error(HQ_ERR_NULL, "W, x, mult, shift and y must be non-null");
+    if (n_vec < 1 || n_vec > 8) return set_error(HQ_ERR_NVEC, "n_vec %d not in [1,8]", n_vec);
+    if (rows < 1 || rows > 0x7fffffffLL || cols < 4 || cols % 4 != 0 || cols > (1LL << 31))
+        return set_error(HQ_ERR_SHAPE, "bad shape rows=%lld cols=%lld (need rows>=1, cols>=4, cols%%4==0)",
+                         (long long)rows, (long long)cols);
+    if (!aligned(W, 16) || !aligned(x, 16) || !aligned(mult, 4) || !aligned(shift, 4))
+        return set_error(HQ_ERR_ALIGN, "W and x must be 16-byte aligned, mult and shift 4-byte aligned");
+    return finish(launch_matvec_i8(W, x, mult, shift, y, rows, cols, n_vec, (cudaStream_t)stream));
+}
+
+hq_status hq_moe_matvec_q8_0(const void *W_bank, const int32_t *expert_ids, const float *x,
+                             int x_per_slot, float *y, int64_t n_experts, int n_active, int64_t rows,
+                             int64_t cols, int n_vec, hq_stream_t stream) {
+    if (!W_bank || !expert_ids || !x || !y) return set_error(HQ_ERR_NULL, "W_bank, expert_ids, x and y must be non-null");
+    if (n_vec < 1 || n_vec > 8) return set_error(HQ_ERR_NVEC, "n_vec %d not in [1,8]", n_vec);
+    if (n_experts < 1 || n_active < 1 || n_active > n_experts || (long long)n_vec * n_active > 256 ||
+        rows < 1 || cols < 256 || cols % 256 != 0 || rows * n_experts > 0x7fffffffLL || cols > (1LL << 31) ||
+        (x_per_slot != 0 && x_per_slot != 1))
+        return set_error(HQ_ERR_SHAPE,
+                         "bad MoE shape n_experts=%lld n_active=%d rows=%lld cols=%lld x_per_slot=%d "
+                         "(need 1<=n_active<=n_experts, n_vec*n_active<=256, cols%%256==0)",
+                         (long long)n_experts, n_active, (long long)rows, (long long)cols, x_per_slot);
+    if (!aligned(W_bank, 16) || !aligned(x, 16) || !aligned(y, 4) || !aligned(expert_ids, 4))
+        return set_error(HQ_ERR_ALIGN, "W_bank and x must be 16-byte aligned");
+    return finish(launch_moe_q8_0(W_bank, expert_ids, x, x_per_slot, y, n_experts, n_active, rows, cols,
+                                  n_vec, (cudaStream_t)stream));
+}
+
+hq_status hq_quantize_q8_0(const float *W, void *out, int64_t rows, int64_t cols, hq_stream_t stream) {
+    if (!W || !out) return set_error(HQ_ERR_NULL, "W and out must be non-null");
+    if (rows < 1 || cols < 32 || cols % 32 != 0) return set_error(HQ_ERR_SHAPE, "need rows>=1, cols%%32==0");
+    if (!aligned(W, 16) || !aligned(out, 2)) return set_error(HQ_ERR_ALIGN, "W must be 16-byte aligned");
+    return finish(launch_quantize(0, W, out, nullptr, rows, cols, (cudaStream_t)stream));
+}
+
+hq_status hq_quantize_q4_0(const float *W, void *out, int64_t rows, int64_t cols, hq_stream_t stream) {
+    if (!W || !out) return set_error(HQ_ERR_NULL, "W and out must be non-null");
+    if (rows < 1 || cols < 32 || cols % 32 != 0) return set_error(HQ_ERR_SHAPE, "need rows>=1, cols%%32==0");
+    if (!aligned(W, 16) || !aligned(out, 2)) return set_error(HQ_ERR_ALIGN, "W must be 16-byte aligned");
+    return finish(launch_quantize(1, W, out, nullptr, rows, cols, (cudaStream_t)stream));
+}
+
+hq_status hq_quantize_i8_rows(const float *W, int8_t *Wq, float *scale, int64_t rows, int64_t cols,
+                              hq_stream_t stream) {
+    if (!W || !Wq || !scale) return set_error(HQ_ERR_NULL, "W, Wq and scale must be non-null");
+    if (rows < 1 || rows > 0x7fffffffLL || cols < 1) return set_error(HQ_ERR_SHAPE, "need rows>=1, cols>=1");
+    if (!aligned(W, 4) || !aligned(scale, 4)) return set_error(HQ_ERR_ALIGN, "W and scale must be 4-byte aligned");
+    return finish(launch_quantize(2, W, Wq, scale, rows, cols, (cudaStream_t)stream));
+}
+
+hq_status hq_requant_params(const double *M, int64_t n, int32_t *mult, int32_t *shift) {
+    if (!M || !mult || !shift) return set_error(HQ_ERR_NULL, "M, mult and shift must be non-null");
+    for (int64_t i = 0; i < n; ++i) {
+        double m = M[i];
+        if (!(m > 0.0 && m < 1.0)) return set_error(HQ_ERR_UNSUPPORTED, "M[%lld] = %g not in (0,1)", (long long)i, m);
+        // double m until it lies in [0.5, 1): each doubling is exact and adds one to the shift
+        int s = 0;
+        while (m < 0.5) { m *= 2.0; ++s; }
+        long long q = llround(m * 2147483648.0);           // m * 2^31, exact before rounding
+        if (q == 2147483648LL) { q = 1073741824LL; --s; }
+        if (s < 0 || s > 31) return set_error(HQ_ERR_UNSUPPORTED, "M[%lld] = %g needs shift %d", (long long)i, M[i], s);
+        mult[i] = (int32_t)q;
+        shift[i] = s;
+    }
+    return finish(HQ_OK);
+}
+
+hq_status hq_requant_i32_debug(const int32_t *acc, const int32_t *mult, const int32_t *shift,
+                               int8_t *y, int64_t n, int64_t rows, hq_stream_t stream) {
+    if (!acc || !mult || !shift || !y) return set_error(HQ_ERR_NULL, "acc, mult, shift and y must be non-null");
+    if (n < 1 || rows < 1) return set_error(HQ_ERR_SHAPE, "need n>=1, rows>=1");
+    return finish(launch_requant_debug(acc, mult, shift, y, n, rows, (cudaStream_t)stream));
+}
+
+hq_status hq_device_fault(uint32_t *fault) {
+    if (!fault) return set_error(HQ_ERR_NULL, "fault must be non-null");
+    DeviceInfo *dev = nullptr;
+    hq_status st = device_info(&dev);
+    if (st != HQ_OK) return st;
+    cudaError_t e = cudaDeviceSynchronize();
+    uint32_t v = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&v, dev->fault, sizeof(v), cudaMemcpyDeviceToHost);
+    const uint32_t zero = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(dev->fault, &zero, sizeof(zero), cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "reading the fault word: %s", cudaGetErrorString(e));
+    *fault = v;
+    if (v) return set_error(HQ_ERR_DEVICE, "device fault word 0x%x", v);
+    return finish(HQ_OK);
+}
+
+}  // extern "C"

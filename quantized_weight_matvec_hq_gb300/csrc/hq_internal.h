@@ -1,0 +1,41 @@
+// hq_internal.h -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hq.h"
+
+namespace hq {
+
+// Per-device state set up once: SM count, the fault word's device address,
+// and the driver's tensor-map encoder.
+struct DeviceInfo {
+    int device = -1;
+    int num_sms = 0;
+    int max_smem_optin = 0;
+    int cc_major = 0, cc_minor = 0;
+    uint32_t *fault = nullptr;
+};
+
+hq_status device_info(DeviceInfo **out);            // current device
+hq_status set_error(hq_status st, const char *fmt, ...);
+void *tensor_map_encoder();                         // PFN_cuTensorMapEncodeTiled
+
+// Launchers (arguments already validated by the API layer).
+hq_status launch_matvec_float_q8_0(const void *W, const float *x, float *y, int64_t rows,
+                                   int64_t cols, int n_vec, cudaStream_t stream);
+hq_status launch_matvec_float_q4_0(const void *W, const float *x, float *y, int64_t rows,
+                                   int64_t cols, int n_vec, cudaStream_t stream);
+hq_status launch_moe_q8_0(const void *W_bank, const int32_t *ids, const float *x, int x_per_slot,
+                          float *y, int64_t n_experts, int n_active, int64_t rows, int64_t cols,
+                          int n_vec, cudaStream_t stream);
+hq_status launch_matvec_i8(const int8_t *W, const int8_t *x, const int32_t *mult,
+                           const int32_t *shift, int8_t *y, int64_t rows, int64_t cols, int n_vec,
+                           cudaStream_t stream);
+hq_status launch_requant_debug(const int32_t *acc, const int32_t *mult, const int32_t *shift,
+                               int8_t *y, int64_t n, int64_t rows, cudaStream_t stream);
+hq_status launch_quantize(int fmt, const float *W, void *out, float *scale, int64_t rows,
+                          int64_t cols, cudaStream_t stream);
+
+}  // namespace hq

@@ -1,0 +1,921 @@
+// hq_kernels.cu -- the quantized-weight matvec kernels for sm_103a:
+// Q8_0 and Q4_0 float matvecs, their MoE (expert-indexed) variant, and the
+// per-output-channel int8 GEMV with gemmlowp requant.
+//
+// What is computed:
+//  * float formats ("One Native Stack for Private, Continuously-Learning AI",
+//    section "The Unified Quant Core" and the Lemma of section "The Central
+//    Efficiency Thesis"): y[v][i] = sum_j d_{i,b(j)} * q_{i,j} * x[v][j] over
+//    the stored blocks, fp32 accumulation, n_vec = 1..8 vectors per pass;
+//  * MoE ("Economical Serving and the hanzo.ai Platform", subsection "One
+//    Quant-Agnostic Core"): every routed expert through the same core;
+//  * int8 ("Blue -- porting zen-nano (Qwen3-0.6B) to deterministic on-chain
+//    inference", section "Quantization recipe (validated)"): int32 sum of
+//    int8 products, then SaturatingRoundingDoublingHighMul and
+//    RoundingDivideByPOT per output channel, saturated to int8.
+//
+// GB300 design (the pages' lane-strided HIP kernel is prior art only):
+//  * HBM-bound: each weight byte is read once per call.  A producer warp
+//    stages weights into shared memory with 2-D TMA tensor copies (one per
+//    stage of 32*R rows x one K chunk), completing on mbarriers, with
+//    evict-first L2 hints; consumer warps never load weights from global.
+//  * Lane l of a consumer warp owns output rows l, l+32, ... of the tile: a
+//    row's partial sum never crosses lanes, and all lanes read the same x
+//    element at once, so x comes from shared memory as broadcasts and is
+//    reused across the R rows a lane holds.
+//  * Bank-conflict-free row reads: a 256-column chunk of a row is 272 B
+//    (Q8_0) or 144 B (Q4_0), an odd number of 16-byte units, so 8 lanes
+//    reading 16-byte units of 8 consecutive rows hit 8 distinct bank groups;
+//    int8 chunks are 128 B with the TMA 128-byte swizzle.
+//  * int8 / nibble -> fp32 without conversion instructions: the byte goes
+//    into the mantissa of 2^23 (prmt), and 2^23 + bias is subtracted exactly
+//    with a packed fp32x2 add; products are packed fp32x2 FMAs.  The block sum
+//    is scaled by the block's fp16 d once per block.
+//  * Matrices with few row tiles split K over a thread-block cluster; the
+//    partial sums are combined through distributed shared memory in a fixed
+//    order (no atomics, so results are deterministic).  Large matrices run
+//    persistent CTAs over row tiles.
+//  * Every wait is bounded (hq_device.cuh); nothing traps.
+#include <cudaTypedefs.h>
+#include <limits.h>
+#include <stdio.h>
+
+#include <algorithm>
+#include <type_traits>
+
+#include "hq_device.cuh"
+#include "hq_internal.h"
+
+#ifndef HQ_PART
+#define HQ_PART 0
+#endif
+#if HQ_PART == 1
+#define HQ_PART_NAME(f) f##_q4_0
+#else
+#define HQ_PART_NAME(f) f##_q8_0
+#endif
+
+namespace hq {
+
+constexpr int kMaxConsWarps = 8;    // consumer warps per CTA
+constexpr int kMaxPairs = 256;      // MoE: n_vec * n_active
+
+// ------------------------------------------------------------------ format policies
+// Each policy states the block geometry, the TMA box of one K chunk of one
+// row, the accumulator type, and the per-chunk decode + multiply-add.
+
+constexpr uint32_t kMagic = 0x4B000000u;                    // fp32 2^23
+
+__device__ __forceinline__ float byte_as_float(uint32_t word, int byte) {
+    // 2^23 + value of byte `byte` of `word`: the byte lands in the low mantissa bits
+    return __uint_as_float(prmt(word, kMagic, 0x7540u | (uint32_t)byte));
+}
+
+struct PolQ8_0 {
+    static constexpr int kBlockBytes = 34;
+    static constexpr int kChunkCols = 256;          // 8 blocks
+    static constexpr int kChunkBytes = 272;         // per row, = 17 x 16 B
+    static constexpr int kBoxInner = 68;            // uint32 words per chunk row
+    static constexpr int kXElemBytes = 4;           // fp32 activations
+    static constexpr bool kSwizzle = false;
+    using Acc = float2;
+    using Red = float;
+
+    // per lane: R rows x one chunk of the stage
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume(const uint8_t *__restrict__ wt,
+                                                   const uint8_t *__restrict__ xt8, int lane,
+                                                   Acc (&acc)[R][NV]) {
+        const float *xt = reinterpret_cast<const float *>(xt8);
+        constexpr int NCH = (R * NV >= 4) ? 1 : 2;               // independent FMA chains
+        const float2 kOff = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+        const uint4 *rowp[R];
+        uint4 c0[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            rowp[r] = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes);
+            c0[r] = rowp[r][0];
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            // window = 16-byte units 2b..2b+2 of the row chunk; block b starts at its byte 2b
+            uint32_t win[R][12];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint4 c1 = rowp[r][2 * b + 1], c2 = rowp[r][2 * b + 2];
+                win[r][0] = c0[r].x; win[r][1] = c0[r].y; win[r][2] = c0[r].z; win[r][3] = c0[r].w;
+                win[r][4] = c1.x; win[r][5] = c1.y; win[r][6] = c1.z; win[r][7] = c1.w;
+                win[r][8] = c2.x; win[r][9] = c2.y; win[r][10] = c2.z; win[r][11] = c2.w;
+                c0[r] = c2;
+            }
+            float2 s[R][NV][NCH];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) s[r][v][c] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                float4 xv[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * b + 4 * g);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float f[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int o = 2 * b + 2 + 4 * g + i;      // window byte of quant 4g+i
+                        f[i] = byte_as_float(win[r][o >> 2] ^ 0x80808080u, o & 3);
+                    }
+                    const float2 q01 = fadd2(make_float2(f[0], f[1]), kOff);
+                    const float2 q23 = fadd2(make_float2(f[2], f[3]), kOff);
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        float2 &sv = s[r][v][g % NCH];
+                        sv = ffma2(q01, make_float2(xv[v].x, xv[v].y), sv);
+                        sv = ffma2(q23, make_float2(xv[v].z, xv[v].w), sv);
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint32_t sw = win[r][b >> 1];               // fp16 d at window byte 2b
+                const unsigned short hb = (b & 1) ? (unsigned short)(sw >> 16) : (unsigned short)(sw & 0xffffu);
+                const float d = __half2float(__ushort_as_half(hb));
+                const float2 dd = make_float2(d, d);
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    float2 t = s[r][v][0];
+                    if (NCH == 2) t = fadd2(t, s[r][v][NCH - 1]);
+                    acc[r][v] = ffma2(dd, t, acc[r][v]);
+                }
+            }
+        }
+    }
+    __device__ __forceinline__ static Red finish(const Acc &a) { return a.x + a.y; }
+};
+
+struct PolQ4_0 {
+    static constexpr int kBlockBytes = 18;
+    static constexpr int kChunkCols = 256;          // 8 blocks
+    static constexpr int kChunkBytes = 144;         // per row, = 9 x 16 B
+    static constexpr int kBoxInner = 36;            // uint32 words per chunk row
+    static constexpr int kXElemBytes = 4;
+    static constexpr bool kSwizzle = false;
+    using Acc = float2;
+    using Red = float;
+
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume(const uint8_t *__restrict__ wt,
+                                                   const uint8_t *__restrict__ xt8, int lane,
+                                                   Acc (&acc)[R][NV]) {
+        const float *xt = reinterpret_cast<const float *>(xt8);
+        constexpr int NCH = (R * NV >= 4) ? 1 : 2;
+        const float2 kOff = make_float2(-8388616.0f, -8388616.0f);  // -(2^23 + 8)
+        const uint4 *rowp[R];
+        uint4 c0[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            rowp[r] = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes);
+            c0[r] = rowp[r][0];
+        }
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            // window = 16-byte units b, b+1; block b starts at its byte 2b
+            uint32_t lo[R][8], hi[R][8], sw[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint4 c1 = rowp[r][b + 1];
+                const uint32_t win[8] = {c0[r].x, c0[r].y, c0[r].z, c0[r].w, c1.x, c1.y, c1.z, c1.w};
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    lo[r][k] = win[k] & 0x0F0F0F0Fu;
+                    hi[r][k] = (win[k] >> 4) & 0x0F0F0F0Fu;
+                }
+                sw[r] = win[b >> 1];
+                c0[r] = c1;
+            }
+            float2 s[R][NV][NCH];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) s[r][v][c] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                float4 xv[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * b + 4 * g);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float f[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int e = 4 * g + i;                  // element of the block
+                        const int o = 2 * b + 2 + (e & 15);       // window byte holding it
+                        const uint32_t src = (e < 16) ? lo[r][o >> 2] : hi[r][o >> 2];
+                        f[i] = byte_as_float(src, o & 3);
+                    }
+                    const float2 q01 = fadd2(make_float2(f[0], f[1]), kOff);
+                    const float2 q23 = fadd2(make_float2(f[2], f[3]), kOff);
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        float2 &sv = s[r][v][g % NCH];
+                        sv = ffma2(q01, make_float2(xv[v].x, xv[v].y), sv);
+                        sv = ffma2(q23, make_float2(xv[v].z, xv[v].w), sv);
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const unsigned short hb = (b & 1) ? (unsigned short)(sw[r] >> 16) : (unsigned short)(sw[r] & 0xffffu);
+                const float d = __half2float(__ushort_as_half(hb));
+                const float2 dd = make_float2(d, d);
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    float2 t = s[r][v][0];
+                    if (NCH == 2) t = fadd2(t, s[r][v][NCH - 1]);
+                    acc[r][v] = ffma2(dd, t, acc[r][v]);
+                }
+            }
+        }
+    }
+    __device__ __forceinline__ static Red finish(const Acc &a) { return a.x + a.y; }
+};
+
+struct PolI8 {
+    static constexpr int kChunkCols = 128;          // one 128-byte swizzle span
+    static constexpr int kChunkBytes = 128;
+    static constexpr int kBoxInner = 128;           // uint8 elements per chunk row
+    static constexpr int kXElemBytes = 1;
+    static constexpr bool kSwizzle = true;
+    using Acc = int;
+    using Red = int;
+
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume(const uint8_t *__restrict__ wt,
+                                                   const uint8_t *__restrict__ xt, int lane,
+                                                   Acc (&acc)[R][NV]) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            int4 xu[NV];
+#pragma unroll
+            for (int v = 0; v < NV; ++v) xu[v] = *reinterpret_cast<const int4 *>(xt + v * kChunkCols + 16 * u);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const int row = lane + 32 * r;
+                // 128-byte swizzle: 16-byte unit u of tile row `row` sits at unit u ^ (row & 7)
+                const int4 w = *reinterpret_cast<const int4 *>(wt + row * kChunkBytes + 16 * (u ^ (row & 7)));
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    acc[r][v] = __dp4a(w.x, xu[v].x, acc[r][v]);
+                    acc[r][v] = __dp4a(w.y, xu[v].y, acc[r][v]);
+                    acc[r][v] = __dp4a(w.z, xu[v].z, acc[r][v]);
+                    acc[r][v] = __dp4a(w.w, xu[v].w, acc[r][v]);
+                }
+            }
+        }
+    }
+    __device__ __forceinline__ static Red finish(const Acc &a) { return a; }
+};
+
+template <class Acc> __device__ __forceinline__ Acc zero_acc();
+template <> __device__ __forceinline__ float2 zero_acc<float2>() { return make_float2(0.f, 0.f); }
+template <> __device__ __forceinline__ int zero_acc<int>() { return 0; }
+
+// gemmlowp requant, restated: SRDHM(a, m) = floor((a*m + 2^30) / 2^31) except
+// a = m = INT32_MIN -> INT32_MAX; RDivByPOT(v, e) = v / 2^e rounded to nearest,
+// ties away from zero; then saturate to int8.
+__device__ __forceinline__ int requant_i8(int acc, int mult, int shift) {
+    long long v;
+    if (acc == INT_MIN && mult == INT_MIN) v = INT_MAX;
+    else v = ((long long)acc * (long long)mult + (1LL << 30)) >> 31;   // arithmetic shift = floor
+    const int e = min(max(shift, 0), 31);
+    if (e > 0) {
+        const long long mag = v < 0 ? -v : v;
+        const long long q = (mag + (1LL << (e - 1))) >> e;
+        v = v < 0 ? -q : q;
+    }
+    return (int)min(max(v, -128LL), 127LL);
+}
+
+// ------------------------------------------------------------------ kernel arguments / layout
+
+struct KArgs {
+    CUtensorMap tmW;          // weights: {inner units per row, total rows}
+    CUtensorMap tmX;          // dense x: {cols, n_vec}
+    void *y;                  // fp32 [n_vec][rows] / MoE [n_vec][n_active][rows] / int8 [n_vec][rows]
+    const float *x;           // MoE: x base, gathered per vector with bulk copies
+    const int32_t *ids;       // MoE: expert ids [n_vec][n_active]
+    const int32_t *mult;      // int8: [rows]
+    const int32_t *shift;     // int8: [rows]
+    uint32_t *fault;
+    long long rows;           // rows of one matrix
+    long long cols;
+    long long n_experts;
+    int n_chunks;             // cols / kChunkCols
+    int num_tiles;            // row tiles of one matrix
+    int cons_warps;           // consumer warps per CTA
+    int stages;               // ring depth per consumer warp
+    int ksplit;               // CTAs per cluster along K (1: persistent over tiles)
+    int n_vec;
+    int n_active;
+    int x_per_slot;
+};
+
+template <class P, int NV, int R>
+struct Layout {
+    static constexpr int TR = 32 * R;                                   // rows per tile
+    static constexpr int WT = TR * P::kChunkBytes;                      // weight tile bytes
+    static constexpr int kAlign = P::kSwizzle ? 1024 : 128;            // TMA destination alignment
+    static constexpr int XT = ((NV * P::kChunkCols * P::kXElemBytes + kAlign - 1) / kAlign) * kAlign;
+    static constexpr int ST = WT + XT;                                  // stage bytes
+    static_assert(WT % kAlign == 0 && ST % kAlign == 0, "stage alignment");
+    __host__ __device__ static size_t red_off(int cw, int s) { return (size_t)cw * s * ST; }
+    __host__ __device__ static size_t part_off(int cw, int s) { return red_off(cw, s) + (size_t)cw * TR * NV * 4; }
+    __host__ __device__ static size_t bar_off(int cw, int s) { return part_off(cw, s) + (size_t)TR * NV * 4; }
+    __host__ __device__ static size_t misc_off(int cw, int s) { return bar_off(cw, s) + (size_t)2 * cw * s * 8; }
+    static constexpr size_t kMiscBytes = 16 + 4 * kMaxPairs * 4 + 16;   // abort flag, MoE tables
+    __host__ __device__ static size_t total(int cw, int s) { return misc_off(cw, s) + kMiscBytes + kAlign; }
+};
+
+// MoE groups: (token, slot) pairs sorted by expert, cut into groups of at most
+// NV pairs sharing one expert; group g covers sorted[gstart[g] .. + gsize[g]).
+struct MoeTables {
+    int *sorted, *gstart, *gsize, *gexpert, *n_groups;
+};
+
+template <class P, bool MOE>
+__device__ __forceinline__ void store_out(const KArgs &a, const MoeTables &mt, int g, int v,
+                                          long long row, typename P::Red val) {
+    if constexpr (std::is_same<typename P::Red, int>::value) {
+        reinterpret_cast<int8_t *>(a.y)[(long long)v * a.rows + row] =
+            (int8_t)requant_i8(val, a.mult[row], a.shift[row]);
+    } else {
+        const long long p = MOE ? (long long)mt.sorted[mt.gstart[g] + v] : (long long)v;
+        reinterpret_cast<float *>(a.y)[p * a.rows + row] = val;
+    }
+}
+
+// ------------------------------------------------------------------ the kernel
+
+template <class P, int NV, int R, bool MOE>
+__global__ void __launch_bounds__(32 * (kMaxConsWarps + 1), (NV * R <= 2) ? 2 : 1)
+matvec_tma_kernel(const __grid_constant__ KArgs a) {
+    using L = Layout<P, NV, R>;
+    using Acc = typename P::Acc;
+    using Red = typename P::Red;
+    constexpr int TR = L::TR, WT = L::WT, ST = L::ST;
+    constexpr int XV = P::kChunkCols * P::kXElemBytes;                  // x bytes per vector per chunk
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + L::kAlign - 1) & ~uintptr_t(L::kAlign - 1));
+    const int CW = a.cons_warps, S = a.stages;
+    Red *red = reinterpret_cast<Red *>(smem + L::red_off(CW, S));
+    Red *part = reinterpret_cast<Red *>(smem + L::part_off(CW, S));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off(CW, S));
+    int *misc = reinterpret_cast<int *>(smem + L::misc_off(CW, S));
+    volatile int *abort_flag = misc;
+    const MoeTables mt{misc + 4, misc + 4 + kMaxPairs, misc + 4 + 2 * kMaxPairs,
+                       misc + 4 + 3 * kMaxPairs, misc + 1};
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int nthreads = blockDim.x;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2 * CW * S; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if constexpr (MOE) {
+        // Group the (token, slot) pairs by expert; every CTA derives the same table.
+        const int P_ = a.n_vec * a.n_active;
+        for (int p = threadIdx.x; p < P_; p += nthreads) {
+            const int e = a.ids[p];
+            const long long ke = (e >= 0 && e < a.n_experts) ? e : a.n_experts;
+            int rank = 0;
+            for (int q = 0; q < P_; ++q) {
+                const int eq = a.ids[q];
+                const long long kq = (eq >= 0 && eq < a.n_experts) ? eq : a.n_experts;
+                rank += (kq < ke) || (kq == ke && q < p);
+            }
+            mt.sorted[rank] = p;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int ng = 0, bad = 0;
+            for (int i = 0; i < P_;) {
+                const int e = a.ids[mt.sorted[i]];
+                if (e < 0 || e >= a.n_experts) { bad = 1; ++i; continue; }
+                int j = i + 1;
+                while (j < P_ && j - i < NV && a.ids[mt.sorted[j]] == e) ++j;
+                mt.gstart[ng] = i; mt.gsize[ng] = j - i; mt.gexpert[ng] = e; ++ng;
+                i = j;
+            }
+            *mt.n_groups = ng;
+            if (bad && blockIdx.x == 0) atomicOr(a.fault, kFaultExpertId);
+        }
+        __syncthreads();
+        if (blockIdx.x == 0) {                     // outputs of invalid ids become NaN
+            for (int p = 0; p < P_; ++p) {
+                const int e = a.ids[p];
+                if (e >= 0 && e < a.n_experts) continue;
+                for (long long r = threadIdx.x; r < a.rows; r += nthreads)
+                    reinterpret_cast<float *>(a.y)[(long long)p * a.rows + r] = __int_as_float(0x7fc00000);
+            }
+        }
+    }
+    __syncthreads();
+
+    const int n_work = MOE ? (*mt.n_groups) * a.num_tiles : a.num_tiles;
+    const bool split = a.ksplit > 1;
+    const int rank = split ? (int)cluster_ctarank() : 0;
+    const int work0 = split ? (int)(blockIdx.x / a.ksplit) : (int)blockIdx.x;
+    const int wstep = split ? max(n_work, 1) : (int)gridDim.x;     // split: one tile per cluster
+    const int k0 = split ? (int)((long long)rank * a.n_chunks / a.ksplit) : 0;
+    const int k1 = split ? (int)((long long)(rank + 1) * a.n_chunks / a.ksplit) : a.n_chunks;
+    const int nloc = k1 - k0;
+
+    if (warp == CW) {
+        // ---------------- producer: one elected lane issues every copy
+        if (lane == 0) {
+            const uint64_t polW = l2_evict_first_policy();
+            const uint64_t polX = l2_evict_last_policy();
+            prefetch_tensormap(&a.tmW);
+            if (!MOE) prefetch_tensormap(&a.tmX);
+            // Warp w consumes local chunks j = w, w+CW, ... of every work item, so
+            // its n-th stage fill is chunk j of item t with n = t*cnt(w) + j/CW.
+            int items = 0;
+            for (int work = work0; work < n_work; work += wstep, ++items) {
+                const int tile = work % a.num_tiles;
+                int m = NV, g = 0;
+                long long row0 = (long long)tile * TR;
+                if (MOE) {
+                    g = work / a.num_tiles;
+                    m = mt.gsize[g];
+                    row0 += (long long)mt.gexpert[g] * a.rows;
+                }
+                for (int j = 0; j < nloc; ++j) {
+                    const int w = j % CW;
+                    const uint32_t cnt = (uint32_t)((nloc - w + CW - 1) / CW);
+                    const uint32_t n = (uint32_t)items * cnt + (uint32_t)(j / CW);
+                    const int s = n % S;
+                    const uint32_t full = smem_u32(&bars[w * S + s]);
+                    const uint32_t empty = smem_u32(&bars[CW * S + w * S + s]);
+                    if (n >= (uint32_t)S) mbar_wait(empty, ((n / S) - 1) & 1, abort_flag, a.fault);
+                    uint8_t *st = smem + (size_t)(w * S + s) * ST;
+                    const int kc = k0 + j;
+                    mbar_arrive_expect_tx(full, WT + m * XV);
+                    tma_load_2d(smem_u32(st), &a.tmW, kc * P::kBoxInner, (int)row0, full, polW);
+                    if (!MOE) {
+                        tma_load_2d(smem_u32(st + WT), &a.tmX, kc * P::kChunkCols, 0, full, polX);
+                    } else {
+                        for (int i = 0; i < m; ++i) {
+                            const int p = mt.sorted[mt.gstart[g] + i];
+                            const long long xr = a.x_per_slot ? p : p / a.n_active;
+                            bulk_load(smem_u32(st + WT + i * XV),
+                                      a.x + xr * a.cols + (long long)kc * P::kChunkCols, XV, full, polX);
+                        }
+                    }
+                }
+            }
+            // no copy may still be landing in shared memory when the CTA exits
+            for (int w = 0; w < CW; ++w) {
+                const uint32_t total = (uint32_t)items * (uint32_t)((nloc - w + CW - 1) / CW);
+                for (int s = 0; s < S; ++s) {
+                    if (total <= (uint32_t)s) continue;
+                    const uint32_t last = total - 1 - ((total - 1 - s) % S);   // last fill of stage s
+                    const uint32_t bar = smem_u32(&bars[w * S + s]);
+                    const unsigned long long t0 = globaltimer();
+                    while (!mbar_try_wait(bar, (last / S) & 1))
+                        if (globaltimer() - t0 > kWaitTimeoutNs) break;
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---------------- consumers
+        uint32_t seq = 0;
+        for (int work = work0; work < n_work; work += wstep) {
+            const int tile = work % a.num_tiles;
+            int m = NV, g = 0;
+            if (MOE) { g = work / a.num_tiles; m = mt.gsize[g]; }
+            Acc acc[R][NV];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int v = 0; v < NV; ++v) acc[r][v] = zero_acc<Acc>();
+            for (int j = warp; j < nloc; j += CW) {
+                const uint32_t n = seq++;
+                const int s = n % S;
+                mbar_wait(smem_u32(&bars[warp * S + s]), (n / S) & 1, abort_flag, a.fault);
+                const uint8_t *st = smem + (size_t)(warp * S + s) * ST;
+                if constexpr (!MOE) {
+                    P::template consume<NV, R>(st, st + WT, lane, acc);
+                } else {
+                    // only the group's m vectors are multiplied
+                    switch (m) {
+#define HQ_MOE_CASE(M_)                                                              \
+    case M_:                                                                         \
+        if constexpr (M_ <= NV) {                                                    \
+            Acc acc_m[R][M_];                                                        \
+            _Pragma("unroll") for (int r = 0; r < R; ++r)                            \
+                _Pragma("unroll") for (int v = 0; v < M_; ++v) acc_m[r][v] = acc[r][v]; \
+            P::template consume<M_, R>(st, st + WT, lane, acc_m);                    \
+            _Pragma("unroll") for (int r = 0; r < R; ++r)                            \
+                _Pragma("unroll") for (int v = 0; v < M_; ++v) acc[r][v] = acc_m[r][v]; \
+        }                                                                            \
+        break;
+                        HQ_MOE_CASE(1) HQ_MOE_CASE(2) HQ_MOE_CASE(3) HQ_MOE_CASE(4)
+                        HQ_MOE_CASE(5) HQ_MOE_CASE(6) HQ_MOE_CASE(7) HQ_MOE_CASE(8)
+#undef HQ_MOE_CASE
+                        default: break;
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&bars[CW * S + warp * S + s]));
+            }
+            // cross-warp reduction of the tile, in fixed warp order
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    red[(warp * NV + v) * TR + lane + 32 * r] = P::finish(acc[r][v]);
+            named_barrier(1, CW * 32);
+            for (int e = threadIdx.x; e < TR * m; e += CW * 32) {
+                const int v = e / TR, rr = e % TR;
+                Red sum = 0;
+                for (int w2 = 0; w2 < CW; ++w2) sum += red[(w2 * NV + v) * TR + rr];
+                const long long row = (long long)tile * TR + rr;
+                if (split) part[v * TR + rr] = sum;
+                else if (row < a.rows) store_out<P, MOE>(a, mt, g, v, row, sum);
+            }
+            named_barrier(1, CW * 32);
+        }
+    }
+
+    if (split) {
+        // K was split across the cluster: CTA `rank` combines its share of the
+        // tile's outputs over all ranks' partials, in rank order, through DSMEM.
+        cluster_sync();
+        const int work = work0;
+        if (work < n_work) {
+            const int tile = work % a.num_tiles;
+            int m = NV, g = 0;
+            if (MOE) { g = work / a.num_tiles; m = mt.gsize[g]; }
+            const int E = TR * m;
+            const int e0 = (int)((long long)rank * E / a.ksplit);
+            const int e1 = (int)((long long)(rank + 1) * E / a.ksplit);
+            for (int e = e0 + threadIdx.x; e < e1; e += nthreads) {
+                const int v = e / TR, rr = e % TR;
+                const uint32_t addr = smem_u32(&part[v * TR + rr]);
+                Red sum = 0;
+                for (int q = 0; q < a.ksplit; ++q) {
+                    const uint32_t ra = map_shared_rank(addr, q);
+                    if constexpr (std::is_same<Red, int>::value) sum += ld_shared_cluster_s32(ra);
+                    else sum += ld_shared_cluster_f32(ra);
+                }
+                const long long row = (long long)tile * TR + rr;
+                if (row < a.rows) store_out<P, MOE>(a, mt, g, v, row, sum);
+            }
+        }
+        cluster_sync();
+    }
+}
+
+// ------------------------------------------------------------------ plain-load kernels
+// Legal shapes whose rows are not 16-byte aligned (cols % 256 != 0, or int8
+// cols % 128 != 0): one warp per row, lanes over blocks, small aligned loads.
+
+template <int FMT>
+__global__ void __launch_bounds__(256)
+matvec_plain_kernel(const uint8_t *__restrict__ W, const float *__restrict__ x, float *__restrict__ y,
+                    long long rows, long long cols, int n_vec) {
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const long long nb = cols / 32;
+    constexpr int bb = FMT == 0 ? 34 : 18;
+    float acc[8];
+    for (int v = 0; v < 8; ++v) acc[v] = 0.f;
+    for (long long b = lane; b < nb; b += 32) {
+        const uint16_t *blk = reinterpret_cast<const uint16_t *>(W + (row * nb + b) * bb);
+        const float d = __half2float(__ushort_as_half(blk[0]));
+        float q[32];
+#pragma unroll
+        for (int h = 0; h < (bb - 2) / 2; ++h) {
+            const uint32_t two = blk[1 + h];
+            if (FMT == 0) {
+                q[2 * h] = (float)(int8_t)(two & 0xff);
+                q[2 * h + 1] = (float)(int8_t)(two >> 8);
+            } else {
+                q[2 * h] = (float)(int)((two & 0xf) - 8);
+                q[2 * h + 16] = (float)(int)(((two >> 4) & 0xf) - 8);
+                q[2 * h + 1] = (float)(int)(((two >> 8) & 0xf) - 8);
+                q[2 * h + 17] = (float)(int)((two >> 12) - 8);
+            }
+        }
+        for (int v = 0; v < n_vec; ++v) {
+            const float *xv = x + (long long)v * cols + b * 32;
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) s = fmaf(q[j], xv[j], s);
+            acc[v] = fmaf(d, s, acc[v]);
+        }
+    }
+    for (int v = 0; v < n_vec; ++v) {
+        float s = acc[v];
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) y[(long long)v * rows + row] = s;
+    }
+}
+
+#if HQ_PART == 2
+__global__ void __launch_bounds__(256)
+matvec_i8_plain_kernel(const int8_t *__restrict__ W, const int8_t *__restrict__ x,
+                       const int32_t *__restrict__ mult, const int32_t *__restrict__ shift,
+                       int8_t *__restrict__ y, long long rows, long long cols, int n_vec) {
+    const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    int acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    const int *w4 = reinterpret_cast<const int *>(W + row * cols);
+    for (long long j = lane; j < cols / 4; j += 32) {
+        const int w = w4[j];
+        for (int v = 0; v < n_vec; ++v)
+            acc[v] = __dp4a(w, reinterpret_cast<const int *>(x + (long long)v * cols)[j], acc[v]);
+    }
+    for (int v = 0; v < n_vec; ++v) {
+        int s = acc[v];
+        for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+        if (lane == 0) y[(long long)v * rows + row] = (int8_t)requant_i8(s, mult[row], shift[row]);
+    }
+}
+
+__global__ void requant_debug_kernel(const int32_t *__restrict__ acc, const int32_t *__restrict__ mult,
+                                     const int32_t *__restrict__ shift, int8_t *__restrict__ y,
+                                     long long n, long long rows) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+         i += (long long)gridDim.x * blockDim.x)
+        y[i] = (int8_t)requant_i8(acc[i], mult[i % rows], shift[i % rows]);
+}
+
+#endif  // HQ_PART == 2
+
+// ------------------------------------------------------------------ host side
+
+namespace {
+
+struct Plan {
+    int cons_warps = 4, stages = 2, ksplit = 1, grid = 1;
+    size_t smem = 0;
+};
+
+hq_status encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, uint64_t inner,
+                    uint64_t outer, uint64_t row_stride_bytes, uint32_t box_inner, uint32_t box_outer,
+                    bool swizzle128) {
+    auto enc = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(tensor_map_encoder());
+    if (!enc) return set_error(HQ_ERR_UNSUPPORTED, "cuTensorMapEncodeTiled is unavailable");
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(HQ_ERR_LAUNCH, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return HQ_OK;
+}
+
+// Launch geometry.  Row tiles are 32*R rows; when there are too few tiles to
+// give every SM work, K is split across a cluster of up to 8 CTAs.
+template <class P, int NV, int R>
+Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks) {
+    using L = Layout<P, NV, R>;
+    Plan p;
+    const long long target = 2LL * dev.num_sms;          // CTAs wanted in flight
+    int ks = 1;
+    while (ks < 8 && n_work * ks < target && n_chunks >= 2 * ks) ks *= 2;
+    p.ksplit = ks;
+    const int chunks_per_cta = (n_chunks + ks - 1) / ks;
+    p.cons_warps = std::max(1, std::min(ks == 1 ? 4 : kMaxConsWarps, chunks_per_cta));
+    const int per_warp = (chunks_per_cta + p.cons_warps - 1) / p.cons_warps;
+    p.stages = (ks == 1) ? 4 : std::max(1, std::min(2, per_warp));
+    const size_t budget = (size_t)dev.max_smem_optin;
+    while (p.stages > 1 && L::total(p.cons_warps, p.stages) > budget / 2) --p.stages;
+    while (p.cons_warps > 1 && L::total(p.cons_warps, p.stages) > budget) --p.cons_warps;
+    p.smem = L::total(p.cons_warps, p.stages);
+    if (ks == 1) {
+        const long long per_sm = std::max<long long>(1, std::min<long long>(2, (long long)(budget / p.smem)));
+        p.grid = (int)std::min<long long>(n_work, (long long)dev.num_sms * per_sm);
+    } else {
+        p.grid = (int)(n_work * ks);
+    }
+    return p;
+}
+
+size_t dev_smem_limit() {
+    DeviceInfo *d = nullptr;
+    return device_info(&d) == HQ_OK ? (size_t)d->max_smem_optin : 0;
+}
+
+template <class P, int NV, int R, bool MOE>
+hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
+    auto kern = matvec_tma_kernel<P, NV, R, MOE>;
+    // the shared-memory opt-in is raised once per device and kernel, before any
+    // stream capture that launches it
+    static int configured[64] = {0};
+    int devi = 0;
+    cudaGetDevice(&devi);
+    cudaError_t e = cudaSuccess;
+    if (devi < 0 || devi >= 64 || configured[devi] < (int)p.smem) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev_smem_limit());
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
+        if (devi >= 0 && devi < 64) configured[devi] = (int)dev_smem_limit();
+    }
+    a.cons_warps = p.cons_warps;
+    a.stages = p.stages;
+    a.ksplit = p.ksplit;
+    if (p.grid <= 0) return HQ_OK;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
+    cfg.blockDim = dim3((unsigned)(32 * (p.cons_warps + 1)), 1, 1);
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    cfg.numAttrs = 0;
+    if (p.ksplit > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)p.ksplit;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+    }
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "matvec launch: %s", cudaGetErrorString(e));
+    return HQ_OK;
+}
+
+template <class P>
+constexpr int rows_per_lane(int nv) { return nv >= 3 ? 2 : 1; }
+
+template <class P, int NV>
+hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y, const int32_t *mult,
+                   const int32_t *shift, long long rows, long long cols, cudaStream_t stream) {
+    constexpr int R = rows_per_lane<P>(NV);
+    constexpr bool kI8 = std::is_same<P, PolI8>::value;
+    KArgs a = {};
+    long long row_bytes;
+    hq_status st;
+    if constexpr (kI8) {
+        row_bytes = cols;
+        st = encode_2d(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)cols, (uint64_t)rows,
+                       (uint64_t)row_bytes, P::kBoxInner, 32 * R, true);
+        if (st != HQ_OK) return st;
+        st = encode_2d(&a.tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, x, (uint64_t)cols, (uint64_t)NV,
+                       (uint64_t)cols, P::kChunkCols, NV, false);
+    } else {
+        row_bytes = cols / 32 * P::kBlockBytes;
+        st = encode_2d(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, (uint64_t)(row_bytes / 4),
+                       (uint64_t)rows, (uint64_t)row_bytes, P::kBoxInner, 32 * R, false);
+        if (st != HQ_OK) return st;
+        st = encode_2d(&a.tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x, (uint64_t)cols, (uint64_t)NV,
+                       (uint64_t)cols * 4, P::kChunkCols, NV, false);
+    }
+    if (st != HQ_OK) return st;
+    a.y = y;
+    a.mult = mult;
+    a.shift = shift;
+    a.fault = dev.fault;
+    a.rows = rows;
+    a.cols = cols;
+    a.n_chunks = (int)(cols / P::kChunkCols);
+    a.num_tiles = (int)((rows + 32 * R - 1) / (32 * R));
+    a.n_vec = NV;
+    const Plan p = make_plan<P, NV, R>(dev, a.num_tiles, a.n_chunks);
+    return launch_tma<P, NV, R, false>(a, p, stream);
+}
+
+template <class P>
+hq_status dense_dispatch(const DeviceInfo &dev, const void *W, const void *x, void *y,
+                         const int32_t *mult, const int32_t *shift, long long rows, long long cols,
+                         int n_vec, cudaStream_t stream) {
+    switch (n_vec) {
+        case 1: return dense_nv<P, 1>(dev, W, x, y, mult, shift, rows, cols, stream);
+        case 2: return dense_nv<P, 2>(dev, W, x, y, mult, shift, rows, cols, stream);
+        case 3: return dense_nv<P, 3>(dev, W, x, y, mult, shift, rows, cols, stream);
+        case 4: return dense_nv<P, 4>(dev, W, x, y, mult, shift, rows, cols, stream);
+        case 5: return dense_nv<P, 5>(dev, W, x, y, mult, shift, rows, cols, stream);
+        case 6: return dense_nv<P, 6>(dev, W, x, y, mult, shift, rows, cols, stream);
+        case 7: return dense_nv<P, 7>(dev, W, x, y, mult, shift, rows, cols, stream);
+        case 8: return dense_nv<P, 8>(dev, W, x, y, mult, shift, rows, cols, stream);
+        default: return set_error(HQ_ERR_NVEC, "n_vec %d not in [1,8]", n_vec);
+    }
+}
+
+template <int NVMAX>
+hq_status moe_nv(const DeviceInfo &dev, const void *W_bank, const int32_t *ids, const float *x,
+                 int x_per_slot, float *y, long long n_experts, int n_active, long long rows,
+                 long long cols, int n_vec, cudaStream_t stream) {
+    using P = PolQ8_0;
+    constexpr int R = 1;
+    KArgs a = {};
+    const long long row_bytes = cols / 32 * P::kBlockBytes;
+    hq_status st = encode_2d(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, W_bank, (uint64_t)(row_bytes / 4),
+                             (uint64_t)(rows * n_experts), (uint64_t)row_bytes, P::kBoxInner, 32 * R, false);
+    if (st != HQ_OK) return st;
+    a.y = y;
+    a.x = x;
+    a.ids = ids;
+    a.fault = dev.fault;
+    a.rows = rows;
+    a.cols = cols;
+    a.n_experts = n_experts;
+    a.n_chunks = (int)(cols / P::kChunkCols);
+    a.num_tiles = (int)((rows + 32 * R - 1) / (32 * R));
+    a.n_vec = n_vec;
+    a.n_active = n_active;
+    a.x_per_slot = x_per_slot;
+    // The group count is only known on the device; plan for the most groups the
+    // pairs can form (every pair its own expert, at most n_experts of them).
+    const long long max_groups = std::min<long long>((long long)n_vec * n_active,
+                                                     n_experts * (((long long)n_vec * n_active + NVMAX - 1) / NVMAX));
+    Plan p = make_plan<P, NVMAX, R>(dev, (long long)a.num_tiles * max_groups, a.n_chunks);
+    if (p.ksplit > 1) p.grid = (int)((long long)a.num_tiles * max_groups * p.ksplit);
+    return launch_tma<P, NVMAX, R, true>(a, p, stream);
+}
+
+}  // namespace
+
+// The public launchers are compiled in four parts (HQ_PART 0..3, one object
+// file each) so that the template instantiations build in parallel.
+#if !defined(HQ_PART) || HQ_PART == 0 || HQ_PART == 1
+hq_status HQ_PART_NAME(launch_matvec_float)(const void *W, const float *x, float *y, int64_t rows,
+                                            int64_t cols, int n_vec, cudaStream_t stream) {
+    constexpr int FMT = (HQ_PART == 1) ? 1 : 0;
+    using P = std::conditional<FMT == 0, PolQ8_0, PolQ4_0>::type;
+    DeviceInfo *dev = nullptr;
+    hq_status st = device_info(&dev);
+    if (st != HQ_OK) return st;
+    if (cols % 256 == 0) return dense_dispatch<P>(*dev, W, x, y, nullptr, nullptr, rows, cols, n_vec, stream);
+    const unsigned grid = (unsigned)((rows + 7) / 8);
+    matvec_plain_kernel<FMT><<<grid, 256, 0, stream>>>((const uint8_t *)W, x, y, rows, cols, n_vec);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "matvec launch: %s", cudaGetErrorString(e));
+    return HQ_OK;
+}
+#endif
+
+#if HQ_PART == 2
+hq_status launch_matvec_i8(const int8_t *W, const int8_t *x, const int32_t *mult,
+                           const int32_t *shift, int8_t *y, int64_t rows, int64_t cols, int n_vec,
+                           cudaStream_t stream) {
+    DeviceInfo *dev = nullptr;
+    hq_status st = device_info(&dev);
+    if (st != HQ_OK) return st;
+    if (cols % 128 == 0)
+        return dense_dispatch<PolI8>(*dev, W, x, y, mult, shift, rows, cols, n_vec, stream);
+    matvec_i8_plain_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(W, x, mult, shift, y, rows, cols, n_vec);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "int8 matvec launch: %s", cudaGetErrorString(e));
+    return HQ_OK;
+}
+
+hq_status launch_requant_debug(const int32_t *acc, const int32_t *mult, const int32_t *shift,
+                               int8_t *y, int64_t n, int64_t rows, cudaStream_t stream) {
+    const long long blocks = std::min<long long>((n + 255) / 256, 65535);
+    requant_debug_kernel<<<(unsigned)std::max<long long>(blocks, 1), 256, 0, stream>>>(acc, mult, shift, y, n, rows);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "requant launch: %s", cudaGetErrorString(e));
+    return HQ_OK;
+}
+#endif
+
+#if HQ_PART == 3
+hq_status launch_moe_q8_0(const void *W_bank, const int32_t *ids, const float *x, int x_per_slot,
+                          float *y, int64_t n_experts, int n_active, int64_t rows, int64_t cols,
+                          int n_vec, cudaStream_t stream) {
+    DeviceInfo *dev = nullptr;
+    hq_status st = device_info(&dev);
+    if (st != HQ_OK) return st;
+    if ((long long)n_vec * n_active > kMaxPairs)
+        return set_error(HQ_ERR_SHAPE, "n_vec * n_active = %lld exceeds %d",
+                         (long long)n_vec * n_active, kMaxPairs);
+    if (cols % 256 != 0)
+        return set_error(HQ_ERR_SHAPE, "MoE needs cols %% 256 == 0 (cols = %lld)", (long long)cols);
+    if (n_vec <= 1) return moe_nv<1>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, stream);
+    if (n_vec <= 2) return moe_nv<2>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, stream);
+    if (n_vec <= 4) return moe_nv<4>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, stream);
+    return moe_nv<8>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, stream);
+}
+#endif
+
+}  // namespace hq

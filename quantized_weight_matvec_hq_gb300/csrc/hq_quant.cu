@@ -1,0 +1,121 @@
+// hq_quant.cu -- the data-preparation step on the GPU: fp32 weights to Q8_0,
+// Q4_0 and per-output-channel int8.
+//
+// Formats: "One Native Stack for Private, Continuously-Learning AI", section
+// "The Unified Quant Core" (Q8_0 = fp16 d + 32 int8 in 34 B, Q4_0 = fp16 d +
+// 16 bytes of nibbles in 18 B, ggml's layouts).  Int8: "Blue -- porting
+// zen-nano (Qwen3-0.6B) to deterministic on-chain inference", section
+// "Quantization recipe (validated)" (s_w[o] = max|W[o,:]|/127, round(W/s_w)).
+//
+// Every decision that turns a float into an integer code is taken in IEEE
+// fp32 with correctly rounded division (no fast-math), so the bytes are the
+// same on any conforming implementation of the same reading.
+#include <cuda_fp16.h>
+#include <math.h>
+
+#include "hq_internal.h"
+
+namespace hq {
+
+// One thread per 32-weight block.
+__global__ void __launch_bounds__(256)
+quantize_q8_0_kernel(const float *__restrict__ W, uint8_t *__restrict__ out, long long n_blocks) {
+    const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= n_blocks) return;
+    const float4 *src = reinterpret_cast<const float4 *>(W + b * 32);
+    float w[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 t = src[i];
+        w[4 * i] = t.x; w[4 * i + 1] = t.y; w[4 * i + 2] = t.z; w[4 * i + 3] = t.w;
+    }
+    float amax = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) amax = fmaxf(amax, fabsf(w[j]));
+    const float d = __fdiv_rn(amax, 127.0f);
+    // a block is 2-byte aligned: store it as 17 halfwords (d, then quant pairs)
+    unsigned short *blk = reinterpret_cast<unsigned short *>(out + b * 34);
+    blk[0] = __half_as_ushort(__float2half_rn(d));
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+        int q0 = 0, q1 = 0;
+        if (d != 0.f) {
+            q0 = max(-127, min(127, (int)roundf(__fdiv_rn(w[j], d))));
+            q1 = max(-127, min(127, (int)roundf(__fdiv_rn(w[j + 1], d))));
+        }
+        blk[1 + j / 2] = (unsigned short)((q0 & 0xff) | ((q1 & 0xff) << 8));
+    }
+}
+
+__global__ void __launch_bounds__(256)
+quantize_q4_0_kernel(const float *__restrict__ W, uint8_t *__restrict__ out, long long n_blocks) {
+    const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= n_blocks) return;
+    const float4 *src = reinterpret_cast<const float4 *>(W + b * 32);
+    float w[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float4 t = src[i];
+        w[4 * i] = t.x; w[4 * i + 1] = t.y; w[4 * i + 2] = t.z; w[4 * i + 3] = t.w;
+    }
+    // the signed element of largest magnitude, first one on ties
+    float amax = 0.f, m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float a = fabsf(w[j]);
+        if (a > amax) { amax = a; m = w[j]; }
+    }
+    const float d = __fdiv_rn(m, -8.0f);
+    unsigned short *blk = reinterpret_cast<unsigned short *>(out + b * 18);
+    blk[0] = __half_as_ushort(__float2half_rn(d));
+    int n[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        n[j] = 8;
+        if (d != 0.f) n[j] = max(0, min(15, (int)floorf(__fadd_rn(__fdiv_rn(w[j], d), 8.5f))));
+    }
+    // byte j = element j (low nibble) | element j+16 (high nibble); two bytes per store
+#pragma unroll
+    for (int j = 0; j < 16; j += 2)
+        blk[1 + j / 2] = (unsigned short)((n[j] | (n[j + 16] << 4)) | ((n[j + 1] | (n[j + 17] << 4)) << 8));
+}
+
+// One CTA per row: scale = max|w|/127, q = round(w/scale) in [-127, 127].
+__global__ void __launch_bounds__(256)
+quantize_i8_rows_kernel(const float *__restrict__ W, int8_t *__restrict__ Wq, float *__restrict__ scale,
+                        long long cols) {
+    const long long row = blockIdx.x;
+    const float *w = W + row * cols;
+    float amax = 0.f;
+    for (long long j = threadIdx.x; j < cols; j += blockDim.x) amax = fmaxf(amax, fabsf(w[j]));
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+    __shared__ float wmax[8];
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = amax;
+    __syncthreads();
+    amax = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) amax = fmaxf(amax, wmax[i]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (threadIdx.x == 0) scale[row] = s;
+    for (long long j = threadIdx.x; j < cols; j += blockDim.x) {
+        int q = 0;
+        if (s != 0.f) q = max(-127, min(127, (int)roundf(__fdiv_rn(w[j], s))));
+        Wq[row * cols + j] = (int8_t)q;
+    }
+}
+
+hq_status launch_quantize(int fmt, const float *W, void *out, float *scale, int64_t rows,
+                          int64_t cols, cudaStream_t stream) {
+    if (fmt == 2) {
+        quantize_i8_rows_kernel<<<(unsigned)rows, 256, 0, stream>>>(W, (int8_t *)out, scale, cols);
+    } else {
+        const long long nb = rows * (cols / 32);
+        const unsigned grid = (unsigned)((nb + 255) / 256);
+        if (fmt == 0) quantize_q8_0_kernel<<<grid, 256, 0, stream>>>(W, (uint8_t *)out, nb);
+        else quantize_q4_0_kernel<<<grid, 256, 0, stream>>>(W, (uint8_t *)out, nb);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "quantize launch: %s", cudaGetErrorString(e));
+    return HQ_OK;
+}
+
+}  // namespace hq

@@ -1,0 +1,324 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bar: quantized bytes, int8 weights and int8 outputs bit-exact; float outputs
+within |y - y_ref| <= 1e-3 * sum_j |w_deq x_j| + 1e-5 per output (the oracle
+accumulates in f64 and returns the |w x| sum).  Inputs are seeded synthetic
+draws (W ~ N(0, 0.02), x ~ N(0, 1)); quantized inputs come from the oracle's
+quantizer, never from the GPU.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from quantized_weight_matvec_hq_gb300 import synthetic
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def hq():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from quantized_weight_matvec_hq_gb300 import build
+    build.build()
+    import quantized_weight_matvec_hq_gb300 as hq
+    hq.hq_device_fault()
+    yield hq
+    assert hq.hq_device_fault() == 0
+
+
+def dev(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+
+def assert_within(y, y_ref, T, what=""):
+    y = np.asarray(y, dtype=np.float64)
+    excess = np.abs(y - y_ref) - (1e-3 * T + 1e-5)
+    if not np.all(excess <= 0):
+        i = np.unravel_index(np.argmax(excess), excess.shape)
+        raise AssertionError(f"{what}: {np.sum(excess > 0)} outputs out of tolerance; worst at {i}: "
+                             f"gpu {y[i]!r} ref {y_ref[i]!r} T {T[i]!r}")
+
+
+def gpu_matvec(hq, fmt, blocks, x, rows, cols, stream=None):
+    n_vec = x.shape[0]
+    y = torch.full((n_vec, rows), float("nan"), dtype=torch.float32, device="cuda")
+    fn = hq.hq_matvec_q8_0 if fmt == "q8_0" else hq.hq_matvec_q4_0
+    fn(dev(blocks), dev(x), y, rows, cols, n_vec, stream=stream)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+def quant(fmt, W):
+    return oracle.quantize_q8_0(W) if fmt == "q8_0" else oracle.quantize_q4_0(W)
+
+
+# ---------------------------------------------------------------- quantizers
+
+def _special_weights(rows, cols, seed):
+    g = synthetic.rng(seed)
+    W = synthetic.weights(g, rows, cols)
+    W[0, :] = 0                                            # all-zero blocks
+    W[1, :32] = np.float32(-1e-30)                         # tiny: d underflows in fp16
+    W[2, 0], W[2, 5] = np.float32(0.8), np.float32(-0.8)   # |max| tie, clamps to 15 in Q4_0
+    W[3, ::7] *= np.float32(300)                           # outliers
+    W[4, :32] = np.float32(0.25)                           # equal elements
+    W[5, :32] = np.arange(32, dtype=np.float32) * np.float32(0.0625) - np.float32(1)  # exact ratios
+    return W
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
+def test_quantizer_bytes_bit_exact(hq, fmt):
+    rows, cols = 301, 1024 + 96
+    W = _special_weights(rows, cols, 31)
+    out = torch.empty((rows, cols // 32 * (34 if fmt == "q8_0" else 18)), dtype=torch.uint8, device="cuda")
+    (hq.hq_quantize_q8_0 if fmt == "q8_0" else hq.hq_quantize_q4_0)(dev(W), out, rows, cols)
+    torch.cuda.synchronize()
+    got, ref = out.cpu().numpy(), quant(fmt, W)
+    bpb = 34 if fmt == "q8_0" else 18
+    g3, r3 = got.reshape(rows, -1, bpb), ref.reshape(rows, -1, bpb)
+    bad_d = np.argwhere(np.any(g3[:, :, :2] != r3[:, :, :2], axis=2))
+    bad_q = np.argwhere(np.any(g3[:, :, 2:] != r3[:, :, 2:], axis=2))
+    assert len(bad_d) == 0 and len(bad_q) == 0, (
+        f"{len(bad_d)} blocks with a different scale (first {bad_d[:3].tolist()}: gpu "
+        f"{g3[tuple(bad_d[0])][:2].tolist() if len(bad_d) else None} ref "
+        f"{r3[tuple(bad_d[0])][:2].tolist() if len(bad_d) else None}), {len(bad_q)} with different quants")
+
+
+def test_quantizer_i8_rows_bit_exact(hq):
+    rows, cols = 97, 3000
+    W = _special_weights(rows, cols, 32)
+    Wq = torch.empty((rows, cols), dtype=torch.int8, device="cuda")
+    s = torch.empty(rows, dtype=torch.float32, device="cuda")
+    hq.hq_quantize_i8_rows(dev(W), Wq, s, rows, cols)
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.quantize_i8_rows(W)
+    assert np.array_equal(Wq.cpu().numpy(), q_ref)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32))
+
+
+# ---------------------------------------------------------------- float matvecs
+
+# (rows, cols): tiles of 32/64 rows with ragged tails; cols % 256 == 0 use the
+# TMA kernel (few row tiles -> K split over a cluster, many -> persistent
+# CTAs); other multiples of 32 use the plain-load kernel.
+SHAPES = [(1, 256), (31, 512), (33, 1024), (100, 4096), (257, 3072), (1000, 2048),
+          (64, 14336), (5000, 256), (7, 32), (45, 96), (130, 320), (64, 992)]
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("rows,cols", SHAPES)
+def test_matvec_parity(hq, fmt, rows, cols):
+    g = synthetic.rng(1000 + rows + cols)
+    W = synthetic.weights(g, rows, cols)
+    blocks = quant(fmt, W)
+    for n_vec in (1, 2, 3, 4, 5, 8) if rows * cols <= 1 << 20 else (1, 4, 8):
+        x = synthetic.activations(g, n_vec, cols)
+        y_ref, T = oracle.matvec(fmt, blocks, x, rows, cols)
+        y = gpu_matvec(hq, fmt, blocks, x, rows, cols)
+        assert_within(y, y_ref, T, f"{fmt} {rows}x{cols} n_vec={n_vec}")
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
+def test_all_n_vec_and_column_independence(hq, fmt):
+    rows, cols = 200, 2048
+    g = synthetic.rng(77)
+    blocks = quant(fmt, synthetic.weights(g, rows, cols))
+    x = synthetic.activations(g, 8, cols)
+    y_ref, T = oracle.matvec(fmt, blocks, x, rows, cols)
+    for n_vec in range(1, 9):
+        y = gpu_matvec(hq, fmt, blocks, x[:n_vec], rows, cols)
+        assert_within(y, y_ref[:n_vec], T[:n_vec], f"{fmt} n_vec={n_vec}")
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
+def test_closed_forms_on_gpu(hq, fmt):
+    rows, cols = 96, 1024
+    g = synthetic.rng(78)
+    W = synthetic.weights(g, rows, cols)
+    W[10] = 0
+    blocks = quant(fmt, W)
+    Wd = oracle.dequant(fmt, blocks, rows, cols)
+    # one-hot x: exactly one column (d*q is exact in fp32, no rounding happens)
+    for j in (0, 33, 511, 1023):
+        e = np.zeros((1, cols), np.float32)
+        e[0, j] = 1
+        y = gpu_matvec(hq, fmt, blocks, e, rows, cols)
+        assert np.array_equal(y[0].astype(np.float64), Wd[:, j])
+    y = gpu_matvec(hq, fmt, blocks, synthetic.activations(g, 2, cols), rows, cols)
+    assert np.all(y[:, 10] == 0)
+
+
+def test_deterministic_and_stream(hq):
+    rows, cols = 4096, 4096
+    g = synthetic.rng(79)
+    blocks = quant("q8_0", synthetic.weights(g, rows, cols))
+    x = synthetic.activations(g, 2, cols)
+    s = torch.cuda.Stream()
+    y1 = gpu_matvec(hq, "q8_0", blocks, x, rows, cols)
+    with torch.cuda.stream(s):
+        y2 = gpu_matvec(hq, "q8_0", blocks, x, rows, cols, stream=s)
+    assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
+
+
+def _sampled_rows(rows, n=24, width=5):
+    starts = np.linspace(0, rows - width, n).astype(int)
+    return [(int(s), int(s) + width) for s in starts]
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("rows,cols", [(14336, 4096), (4096, 14336), (1024, 4096)])
+def test_full_size_8b_shapes_sampled(hq, fmt, rows, cols):
+    """The 8B-dense decode shapes at full size, in the bench's launch
+    configuration; the oracle computes sampled rows one range at a time."""
+    g = synthetic.rng(synthetic.SEED_BASE + 2)
+    W = synthetic.weights(g, rows, cols)
+    blocks = quant(fmt, W)
+    del W
+    for n_vec in (1, 2, 4, 8):
+        x = synthetic.activations(g, n_vec, cols)
+        y = gpu_matvec(hq, fmt, blocks, x, rows, cols)
+        assert np.all(np.isfinite(y))
+        for lo, hi in _sampled_rows(rows):
+            y_ref, T = oracle.matvec_rows(fmt, blocks, x, rows, cols, lo, hi)
+            assert_within(y[:, lo:hi], y_ref, T, f"{fmt} {rows}x{cols} n_vec={n_vec} rows {lo}:{hi}")
+
+
+def test_full_size_lm_heads_sampled(hq):
+    """The tied Qwen3-0.6B lm_head (151936 x 1024) and the 8B lm_head
+    (128256 x 4096, 558 MB of Q8_0), n_vec = 1, sampled rows."""
+    for rows, cols in ((151936, 1024), (128256, 4096)):
+        g = synthetic.rng(synthetic.SEED_BASE + 7)
+        blocks = np.empty((rows, cols // 32 * 34), np.uint8)
+        step = 8192
+        for r0 in range(0, rows, step):                    # quantize in slabs to bound host memory
+            r1 = min(rows, r0 + step)
+            blocks[r0:r1] = oracle.quantize_q8_0(synthetic.weights(g, r1 - r0, cols))
+        x = synthetic.activations(g, 1, cols)
+        y = gpu_matvec(hq, "q8_0", blocks, x, rows, cols)
+        for lo, hi in _sampled_rows(rows, n=40):
+            y_ref, T = oracle.matvec_rows("q8_0", blocks, x, rows, cols, lo, hi)
+            assert_within(y[:, lo:hi], y_ref, T, f"lm_head {rows}x{cols} rows {lo}:{hi}")
+
+
+# ---------------------------------------------------------------- int8 requant
+
+@pytest.mark.parametrize("rows,cols", [(1024, 3072), (3072, 1024), (77, 100), (40, 4), (300, 640),
+                                       (50, 200), (33, 128)])
+def test_int8_requant_bit_exact(hq, rows, cols):
+    g = synthetic.rng(2000 + rows + cols)
+    W = synthetic.weights(g, rows, cols)
+    x = synthetic.activations(g, 8, cols)
+    Wq, xq, mult, shift = oracle.int8_workload(W, x)
+    for n_vec in (1, 2, 3, 4, 8):
+        y_ref, _ = oracle.matvec_i8_requant(Wq, xq[:n_vec], mult, shift)
+        y = torch.full((n_vec, rows), 99, dtype=torch.int8, device="cuda")
+        hq.hq_matvec_i8_requant(dev(Wq), dev(xq[:n_vec]), dev(mult), dev(shift), y, rows, cols, n_vec)
+        torch.cuda.synchronize()
+        assert np.array_equal(y.cpu().numpy(), y_ref), f"int8 {rows}x{cols} n_vec={n_vec}"
+
+
+def test_int8_extreme_weights_bit_exact(hq):
+    """All +-127 weights and activations: the largest accumulators the path can form."""
+    rows, cols = 64, 3072
+    g = np.random.Generator(np.random.PCG64(5))
+    Wq = np.where(g.random((rows, cols)) < 0.5, -127, 127).astype(np.int8)
+    Wq[0] = 127
+    xq = np.full((2, cols), 127, np.int8)
+    xq[1] = -127
+    mult = g.integers(2 ** 30, 2 ** 31 - 1, size=rows, dtype=np.int64).astype(np.int32)
+    shift = g.integers(0, 32, size=rows).astype(np.int32)
+    y_ref, _ = oracle.matvec_i8_requant(Wq, xq, mult, shift)
+    y = torch.empty((2, rows), dtype=torch.int8, device="cuda")
+    hq.hq_matvec_i8_requant(dev(Wq), dev(xq), dev(mult), dev(shift), y, rows, cols, 2)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), y_ref)
+
+
+def test_requant_epilogue_edge_values(hq):
+    I32_MIN, I32_MAX = -(2 ** 31), 2 ** 31 - 1
+    g = np.random.Generator(np.random.PCG64(6))
+    acc = np.concatenate([np.array([I32_MIN, I32_MIN + 1, -1, 0, 1, I32_MAX - 1, I32_MAX,
+                                    2 ** 30, -(2 ** 30), -(2 ** 30) - 1], np.int64),
+                          g.integers(I32_MIN, I32_MAX, 50000, endpoint=True, dtype=np.int64)]).astype(np.int32)
+    rows = 64
+    mult = g.integers(I32_MIN, I32_MAX, rows, endpoint=True, dtype=np.int64).astype(np.int32)
+    mult[:4] = [I32_MIN, I32_MAX, 0, 1]
+    shift = g.integers(0, 32, rows).astype(np.int32)
+    shift[:3] = [0, 31, 1]
+    y = torch.empty(acc.size, dtype=torch.int8, device="cuda")
+    hq.hq_requant_i32_debug(dev(acc), dev(mult), dev(shift), y, acc.size, rows)
+    torch.cuda.synchronize()
+    assert np.array_equal(y.cpu().numpy(), oracle.requant_array(acc, mult, shift))
+
+
+# ---------------------------------------------------------------- MoE
+
+def _moe_case(n_experts, n_active, rows, cols, n_vec, seed, x_per_slot, ids=None):
+    g = synthetic.rng(seed)
+    bank = np.empty((n_experts * rows, cols // 32 * 34), np.uint8)
+    for e in range(n_experts):
+        bank[e * rows:(e + 1) * rows] = oracle.quantize_q8_0(synthetic.weights(g, rows, cols))
+    if ids is None:
+        ids = synthetic.expert_ids(g, n_vec, n_active, n_experts)
+    x = synthetic.activations(g, n_vec * (n_active if x_per_slot else 1), cols)
+    return bank, ids, x
+
+
+def gpu_moe(hq, bank, ids, x, x_per_slot, n_experts, n_active, rows, cols, n_vec):
+    y = torch.full((n_vec, n_active, rows), -7.0, dtype=torch.float32, device="cuda")
+    hq.hq_moe_matvec_q8_0(dev(bank), dev(ids), dev(x), int(x_per_slot), y, n_experts, n_active, rows, cols, n_vec)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("x_per_slot,rows,cols", [(False, 768, 2048), (True, 2048, 768)])
+@pytest.mark.parametrize("n_vec", [1, 4, 8])
+def test_moe_128_experts_top8(hq, x_per_slot, rows, cols, n_vec):
+    n_experts, n_active = 128, 8
+    bank, ids, x = _moe_case(n_experts, n_active, rows, cols, n_vec, 3000 + n_vec, x_per_slot)
+    y = gpu_moe(hq, bank, ids, x, x_per_slot, n_experts, n_active, rows, cols, n_vec)
+    y_ref, T = oracle.moe_matvec_q8_0(bank, ids, x, x_per_slot, n_experts, n_active, rows, cols, n_vec)
+    assert_within(y, y_ref, T, f"moe n_vec={n_vec} x_per_slot={x_per_slot}")
+
+
+def test_moe_shared_and_duplicate_experts(hq):
+    n_experts, n_active, rows, cols, n_vec = 6, 3, 40, 256, 5
+    ids = np.array([[0, 1, 2], [2, 1, 0], [5, 5, 5], [2, 2, 3], [4, 0, 2]], dtype=np.int32)
+    for x_per_slot in (False, True):
+        bank, ids_, x = _moe_case(n_experts, n_active, rows, cols, n_vec, 4000, x_per_slot, ids=ids)
+        y = gpu_moe(hq, bank, ids_, x, x_per_slot, n_experts, n_active, rows, cols, n_vec)
+        y_ref, T = oracle.moe_matvec_q8_0(bank, ids_, x, x_per_slot, n_experts, n_active, rows, cols, n_vec)
+        assert_within(y, y_ref, T, f"moe duplicates x_per_slot={x_per_slot}")
+
+
+def test_moe_all_same_expert_equals_dense(hq):
+    """Every slot routed to one expert: each slot equals the dense matvec of that
+    expert (to the float tolerance; the grouped kernel sums in another order),
+    and two calls give bit-identical outputs."""
+    n_experts, n_active, rows, cols, n_vec = 4, 2, 100, 512, 3
+    bank, _, x = _moe_case(n_experts, n_active, rows, cols, n_vec, 4001, False)
+    ids = np.full((n_vec, n_active), 3, np.int32)
+    y = gpu_moe(hq, bank, ids, x, False, n_experts, n_active, rows, cols, n_vec)
+    y_again = gpu_moe(hq, bank, ids, x, False, n_experts, n_active, rows, cols, n_vec)
+    assert np.array_equal(y.view(np.uint32), y_again.view(np.uint32))
+    expert = bank[3 * rows:4 * rows]
+    y_dense = gpu_matvec(hq, "q8_0", expert, x, rows, cols)
+    y_ref, T = oracle.matvec("q8_0", expert, x, rows, cols)
+    assert_within(y_dense, y_ref, T, "dense expert 3")
+    for k in range(n_active):
+        assert_within(y[:, k], y_ref, T, f"moe slot {k}")
+
+
+def test_moe_invalid_id_sets_fault_and_nan(hq):
+    n_experts, n_active, rows, cols, n_vec = 4, 2, 64, 256, 2
+    bank, _, x = _moe_case(n_experts, n_active, rows, cols, n_vec, 4002, False)
+    ids = np.array([[1, 9], [3, -1]], dtype=np.int32)
+    y = gpu_moe(hq, bank, ids, x, False, n_experts, n_active, rows, cols, n_vec)
+    assert hq.hq_device_fault() == hq.HQ_FAULT_EXPERT_ID
+    assert np.all(np.isnan(y[0, 1])) and np.all(np.isnan(y[1, 1]))
+    ok = np.array([[1, 0], [3, 0]], dtype=np.int32)
+    y_ref, T = oracle.moe_matvec_q8_0(bank, ok, x, False, n_experts, n_active, rows, cols, n_vec)
+    assert_within(y[:, 0], y_ref[:, 0], T[:, 0], "valid slots beside invalid ones")
+    assert hq.hq_device_fault() == 0
