@@ -47,7 +47,15 @@ WORKLOADS = {
 }
 
 
-def workload_matrices(name):
+def workload_matrices(name, shape=None, fmt=None):
+    """(model, format, [(name, rows, cols), ...]) of one step.  With `shape`
+    ("ROWSxCOLS"), the step is enough distinct copies of that one matrix to
+    exceed 4x the L2 (>= 520 MB) so that no launch reads from L2."""
+    if shape:
+        rows, cols = (int(v) for v in shape.lower().split("x"))
+        one = weight_bytes(fmt, rows, cols)
+        copies = max(4, -(-520_000_000 // one))
+        return f"single {rows}x{cols}", fmt, [(f"m{rows}x{cols}", rows, cols)] * copies
     model, fmt = WORKLOADS[name]
     return model, fmt, synthetic.decode_token_shapes(model)
 
@@ -144,12 +152,12 @@ def _cudart():
 class Step:
     """One decode token's matvecs, resident in HBM, launched through the C ABI."""
 
-    def __init__(self, name, n_vec, device, seed):
+    def __init__(self, name, n_vec, device, seed, shape=None, fmt=None):
         import torch
         import quantized_weight_matvec_hq_gb300 as hq
         self.hq = hq
         self.torch = torch
-        self.model, self.fmt, self.shapes = workload_matrices(name)
+        self.model, self.fmt, self.shapes = workload_matrices(name, shape, fmt)
         self.n_vec = n_vec
         self.device = device
         g = torch.Generator(device=device)
@@ -294,6 +302,9 @@ def main():
     ap.add_argument("--impl", choices=["hq", "reference"], default="hq")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="8b-q8_0")
     ap.add_argument("--n-vec", type=int, default=1)
+    ap.add_argument("--shape", default=None,
+                    help="time one matrix shape ROWSxCOLS instead of a decode token (profiling aid)")
+    ap.add_argument("--format", choices=["q8_0", "q4_0"], default="q8_0", help="format for --shape")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic-file", default=os.path.join(ROOT, "profiles", "traffic.json"),
@@ -303,9 +314,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
-    model, fmt, shapes = workload_matrices(args.workload)
-    config = {"workload": f"{model} decode token, {fmt}, n_vec={args.n_vec}: "
-                          f"{len(shapes)} matvecs (all projections + lm_head)",
+    model, fmt, shapes = workload_matrices(args.workload, args.shape, args.format)
+    config = {"workload": (f"{model} decode token, {fmt}, n_vec={args.n_vec}: "
+                           f"{len(shapes)} matvecs (all projections + lm_head)") if not args.shape else
+                          (f"{len(shapes)} distinct {args.shape} {fmt} matrices per step, n_vec={args.n_vec}"),
               "model_shape": model, "format": fmt, "n_vec": args.n_vec, "matvecs_per_step": len(shapes),
               "l2": "inputs larger than L2 (all weights distinct, 7.97 GB Q8_0 / 4.2 GB Q4_0 per step)"
               if model == "8b-dense" else "all weights distinct per step",
@@ -343,7 +355,7 @@ def main():
     device = torch.device("cuda", local_rank)
     torch.cuda.set_device(device)
 
-    step = Step(args.workload, args.n_vec, device, synthetic.SEED_BASE + 2 + rank)
+    step = Step(args.workload, args.n_vec, device, synthetic.SEED_BASE + 2 + rank, args.shape, args.format)
     graph = step.capture()
     events = LaunchEvents(len(shapes), _cudart())
     graph_ev = step.capture(events)
@@ -448,7 +460,7 @@ def main():
         "gpu_launches": len(shapes) * args.steps,
         "clocks": clk,
     }
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not args.shape:
         gbs, desc, el = OracleSample(args.workload, args.n_vec).timed(args.cpu_budget)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": desc, "seconds": round(el, 2)}

@@ -192,7 +192,9 @@ hq_status hq_requant_i32_debug(const int32_t *acc, const int32_t *mult, const in
  * in a per-device word and the kernel finishes without using the missing
  * data.  hq_device_fault() synchronizes the current device, returns the word
  * in *fault (0 = none) and clears it; it returns HQ_ERR_DEVICE if the word
- * was non-zero.
+ * was non-zero.  Bits 0..7 are the HQ_FAULT_* flags; when the first fault of
+ * the word was a timeout, bits 9..31 hold the index of the CTA that gave up
+ * and bit 8 is set if the waiter was a consumer warp (clear: the producer).
  */
 #define HQ_FAULT_WAIT_TIMEOUT 1u   /* an mbarrier wait exceeded its time limit */
 #define HQ_FAULT_EXPERT_ID    2u   /* an expert id outside [0, n_experts)      */

@@ -210,7 +210,8 @@ hq_status hq_device_fault(uint32_t *fault) {
     if (e == cudaSuccess) e = cudaMemcpy(dev->fault, &zero, sizeof(zero), cudaMemcpyHostToDevice);
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "reading the fault word: %s", cudaGetErrorString(e));
     *fault = v;
-    if (v) return set_error(HQ_ERR_DEVICE, "device fault word 0x%x", v);
+    if (v) return set_error(HQ_ERR_DEVICE, "device fault word 0x%x (flags 0x%x, CTA %u, %s)", v, v & 0xffu,
+                            v >> 9, (v & 0x100u) ? "consumer" : "producer");
     return finish(HQ_OK);
 }
 

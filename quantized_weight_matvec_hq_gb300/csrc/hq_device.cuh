@@ -10,9 +10,12 @@
 
 namespace hq {
 
-// A wait that has not completed after this long gives up, sets the fault word
-// and the kernel finishes without the missing data (it never hangs or traps).
-constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;   // 2 s
+// A wait that has not completed after this many SM cycles (about 2 s at the
+// GB300's clocks) gives up, sets the fault word and the kernel finishes
+// without the missing data (it never hangs or traps).  The SM cycle counter is
+// used, not %globaltimer: the global timer was seen to jump forward by seconds
+// when a kernel starts after the GPU has been idle.
+constexpr long long kWaitTimeoutCycles = 4000000000ll;
 constexpr uint32_t kFaultWaitTimeout = 1u;
 constexpr uint32_t kFaultExpertId = 2u;
 
@@ -20,11 +23,7 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
+__device__ __forceinline__ long long sm_cycles() { return clock64(); }
 
 // ------------------------------------------------------------------ mbarrier
 
@@ -55,24 +54,95 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in hardware (up to `ns`) until the
+// phase completes, instead of spinning on the issue slots other warps need.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity), "r"(ns) : "memory");
+    return ok != 0;
+}
+
 // Bounded wait on phase `parity` of an mbarrier.  `abort` is CTA-shared: once
-// any wait in the CTA (or the fault word of any CTA) has given up, later waits
-// return false at once so the kernel drains in bounded time.
+// any wait in the CTA (or, through the fault word, in any CTA) has timed out,
+// later waits return false at once so the kernel drains in bounded time.  The clock and
+// the global fault word are only looked at every 256 polls, so a waiting warp
+// notices a completed phase within one poll.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
                                           volatile int *abort, uint32_t *fault) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = sm_cycles();
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
-    unsigned long long t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if ((it & 15u) == 0) {
+            if (*abort) return false;
+            // only another wait's timeout aborts; a data fault (bad expert id) does not
+            if (*(volatile uint32_t *)fault & kFaultWaitTimeout) { *abort = 1; return false; }
+            if (sm_cycles() - t0 > kWaitTimeoutCycles) {
+                // bits 8..31 keep where the first timeout happened: the CTA and
+                // whether the waiter was a consumer (bit 8 set) or the producer
+                const uint32_t site = ((blockIdx.x & 0x7fffffu) << 9) | ((threadIdx.x < 128u) ? 0x100u : 0u);
+                atomicCAS(fault, 0u, site | kFaultWaitTimeout);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// try_wait with acquire at cluster scope: sees the stores that remote CTAs
+// released before arriving.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void st_shared_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_shared_cluster_s32(uint32_t addr, int v) {
+    asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+// As mbar_wait, with cluster-scope acquire (for barriers other CTAs arrive on).
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int *abort, uint32_t *fault) {
+    const long long t0 = sm_cycles();
 #pragma unroll 1
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort || *(volatile uint32_t *)fault) { *abort = 1; return false; }
-        if (globaltimer() - t0 > kWaitTimeoutNs) {
-            atomicOr(fault, kFaultWaitTimeout);
-            *abort = 1;
-            return false;
+    for (uint32_t it = 0;; ++it) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((it & 255u) == 255u) {
+            if (*abort) return false;
+            if (*(volatile uint32_t *)fault & kFaultWaitTimeout) { *abort = 1; return false; }
+            if (sm_cycles() - t0 > kWaitTimeoutCycles) {
+                const uint32_t site = ((blockIdx.x & 0x7fffffu) << 9) | 0x100u;
+                atomicCAS(fault, 0u, site | kFaultWaitTimeout);
+                *abort = 1;
+                return false;
+            }
         }
     }
 }

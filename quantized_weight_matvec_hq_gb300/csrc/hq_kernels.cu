@@ -39,6 +39,7 @@
 #include <cudaTypedefs.h>
 #include <limits.h>
 #include <stdio.h>
+#include <stdlib.h>
 
 #include <algorithm>
 #include <type_traits>
@@ -57,7 +58,6 @@
 
 namespace hq {
 
-constexpr int kMaxConsWarps = 8;    // consumer warps per CTA
 constexpr int kMaxPairs = 256;      // MoE: n_vec * n_active
 
 // ------------------------------------------------------------------ format policies
@@ -77,12 +77,13 @@ struct PolQ8_0 {
     static constexpr int kChunkBytes = 272;         // per row, = 17 x 16 B
     static constexpr int kBoxInner = 68;            // uint32 words per chunk row
     static constexpr int kXElemBytes = 4;           // fp32 activations
+    static constexpr int kUnits = 8;                // blocks per chunk, split across consumer warps
     static constexpr bool kSwizzle = false;
     using Acc = float2;
     using Red = float;
 
-    // per lane: R rows x one chunk of the stage
-    template <int NV, int R>
+    // per lane: R rows x blocks [B0, B0+NB) of one chunk of the stage
+    template <int NV, int R, int B0, int NB>
     __device__ __forceinline__ static void consume(const uint8_t *__restrict__ wt,
                                                    const uint8_t *__restrict__ xt8, int lane,
                                                    Acc (&acc)[R][NV]) {
@@ -94,10 +95,10 @@ struct PolQ8_0 {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             rowp[r] = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes);
-            c0[r] = rowp[r][0];
+            c0[r] = rowp[r][2 * B0];
         }
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
+        for (int b = B0; b < B0 + NB; ++b) {
             // window = 16-byte units 2b..2b+2 of the row chunk; block b starts at its byte 2b
             uint32_t win[R][12];
 #pragma unroll
@@ -163,11 +164,12 @@ struct PolQ4_0 {
     static constexpr int kChunkBytes = 144;         // per row, = 9 x 16 B
     static constexpr int kBoxInner = 36;            // uint32 words per chunk row
     static constexpr int kXElemBytes = 4;
+    static constexpr int kUnits = 8;
     static constexpr bool kSwizzle = false;
     using Acc = float2;
     using Red = float;
 
-    template <int NV, int R>
+    template <int NV, int R, int B0, int NB>
     __device__ __forceinline__ static void consume(const uint8_t *__restrict__ wt,
                                                    const uint8_t *__restrict__ xt8, int lane,
                                                    Acc (&acc)[R][NV]) {
@@ -179,10 +181,10 @@ struct PolQ4_0 {
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             rowp[r] = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes);
-            c0[r] = rowp[r][0];
+            c0[r] = rowp[r][B0];
         }
 #pragma unroll
-        for (int b = 0; b < 8; ++b) {
+        for (int b = B0; b < B0 + NB; ++b) {
             // window = 16-byte units b, b+1; block b starts at its byte 2b
             uint32_t lo[R][8], hi[R][8], sw[R];
 #pragma unroll
@@ -252,16 +254,17 @@ struct PolI8 {
     static constexpr int kChunkBytes = 128;
     static constexpr int kBoxInner = 128;           // uint8 elements per chunk row
     static constexpr int kXElemBytes = 1;
+    static constexpr int kUnits = 8;                // 16-byte units per chunk
     static constexpr bool kSwizzle = true;
     using Acc = int;
     using Red = int;
 
-    template <int NV, int R>
+    template <int NV, int R, int U0, int NU>
     __device__ __forceinline__ static void consume(const uint8_t *__restrict__ wt,
                                                    const uint8_t *__restrict__ xt, int lane,
                                                    Acc (&acc)[R][NV]) {
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = U0; u < U0 + NU; ++u) {
             int4 xu[NV];
 #pragma unroll
             for (int v = 0; v < NV; ++v) xu[v] = *reinterpret_cast<const int4 *>(xt + v * kChunkCols + 16 * u);
@@ -305,6 +308,9 @@ __device__ __forceinline__ int requant_i8(int acc, int mult, int shift) {
 
 // ------------------------------------------------------------------ kernel arguments / layout
 
+constexpr int kConsWarps = 2;       // consumer warps per CTA; warp w takes the fills n = w mod 2
+constexpr int kMaxSplit = 8;        // CTAs per cluster when K is split
+
 struct KArgs {
     CUtensorMap tmW;          // weights: {inner units per row, total rows}
     CUtensorMap tmX;          // dense x: {cols, n_vec}
@@ -319,15 +325,14 @@ struct KArgs {
     long long n_experts;
     int n_chunks;             // cols / kChunkCols
     int num_tiles;            // row tiles of one matrix
-    int cons_warps;           // consumer warps per CTA
-    int stages;               // ring depth per consumer warp
+    int stages;               // depth of the CTA's stage ring
     int ksplit;               // CTAs per cluster along K (1: persistent over tiles)
     int n_vec;
     int n_active;
     int x_per_slot;
 };
 
-template <class P, int NV, int R>
+template <class P, int NV, int R, bool MOE>
 struct Layout {
     static constexpr int TR = 32 * R;                                   // rows per tile
     static constexpr int WT = TR * P::kChunkBytes;                      // weight tile bytes
@@ -335,12 +340,12 @@ struct Layout {
     static constexpr int XT = ((NV * P::kChunkCols * P::kXElemBytes + kAlign - 1) / kAlign) * kAlign;
     static constexpr int ST = WT + XT;                                  // stage bytes
     static_assert(WT % kAlign == 0 && ST % kAlign == 0, "stage alignment");
-    __host__ __device__ static size_t red_off(int cw, int s) { return (size_t)cw * s * ST; }
-    __host__ __device__ static size_t part_off(int cw, int s) { return red_off(cw, s) + (size_t)cw * TR * NV * 4; }
-    __host__ __device__ static size_t bar_off(int cw, int s) { return part_off(cw, s) + (size_t)TR * NV * 4; }
-    __host__ __device__ static size_t misc_off(int cw, int s) { return bar_off(cw, s) + (size_t)2 * cw * s * 8; }
-    static constexpr size_t kMiscBytes = 16 + 4 * kMaxPairs * 4 + 16;   // abort flag, MoE tables
-    __host__ __device__ static size_t total(int cw, int s) { return misc_off(cw, s) + kMiscBytes + kAlign; }
+    static constexpr size_t kMiscBytes = 16 + (MOE ? 4 * kMaxPairs * 4 : 0);   // abort flag, MoE tables
+    __host__ __device__ static size_t red_off(int s) { return (size_t)s * ST; }
+    __host__ __device__ static size_t part_off(int s) { return red_off(s) + (size_t)kConsWarps * TR * NV * 4; }
+    __host__ __device__ static size_t bar_off(int s) { return part_off(s) + (size_t)kMaxSplit * TR * NV * 4; }
+    __host__ __device__ static size_t misc_off(int s) { return bar_off(s) + (size_t)(2 * s + 2) * 8; }
+    __host__ __device__ static size_t total(int s) { return misc_off(s) + kMiscBytes + kAlign; }
 };
 
 // MoE groups: (token, slot) pairs sorted by expert, cut into groups of at most
@@ -361,37 +366,92 @@ __device__ __forceinline__ void store_out(const KArgs &a, const MoeTables &mt, i
     }
 }
 
+// A whole chunk for one warp, in pieces of two units; the empty asm between
+// pieces keeps the compiler from hoisting every piece's shared loads at once
+// (which would cost registers and occupancy, not latency).
+template <class P, int NV, int R>
+__device__ __forceinline__ void consume_chunk(const uint8_t *wt, const uint8_t *xt, int lane,
+                                              typename P::Acc (&acc)[R][NV]) {
+    P::template consume<NV, R, 0, 2>(wt, xt, lane, acc);
+    asm volatile("" ::: "memory");
+    P::template consume<NV, R, 2, 2>(wt, xt, lane, acc);
+    asm volatile("" ::: "memory");
+    P::template consume<NV, R, 4, 2>(wt, xt, lane, acc);
+    asm volatile("" ::: "memory");
+    P::template consume<NV, R, 6, 2>(wt, xt, lane, acc);
+}
+
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int c0, int c1) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1) : "memory");
+}
+
 // ------------------------------------------------------------------ the kernel
+//
+// CTA = 4 consumer warps + 1 producer warp, several CTAs per SM (each with its
+// own producer: one thread issuing copies cannot keep HBM busy for a whole
+// SM).  The producer walks the CTA's work items (row tiles, or (expert group,
+// row tile) for MoE) and fills one stage of the CTA's ring per K chunk.
+// Fill n (chunk j of a tile, counted over the CTA's items) lands in stage
+// n mod S and is consumed whole by warp n mod CW, which owns the tile's 32*R
+// rows (one per lane); S is a multiple of CW, so every stage has one owner.  A tile ends with a fixed-order reduction over the four
+// warps; with a K split, the CTAs of a cluster then combine their partials
+// through DSMEM.
+//
+// Programmatic dependent launch: the kernel lets the next one in the stream
+// start as soon as it is resident, prefetches its first weight tiles into L2
+// (weights are never written by another kernel), and waits for the previous
+// kernel only before it touches x or y.
+
+// CTAs per SM the kernel is compiled for: 4 when a lane holds few accumulators
+// (96 registers), 2 when it holds many.
+template <int NV, int R>
+constexpr int ctas_per_sm() { return (NV * R <= 2) ? 5 : 3; }
 
 template <class P, int NV, int R, bool MOE>
-__global__ void __launch_bounds__(32 * (kMaxConsWarps + 1), (NV * R <= 2) ? 2 : 1)
+__global__ void __launch_bounds__(32 * (kConsWarps + 1), ctas_per_sm<NV, R>())
 matvec_tma_kernel(const __grid_constant__ KArgs a) {
-    using L = Layout<P, NV, R>;
+    using L = Layout<P, NV, R, MOE>;
     using Acc = typename P::Acc;
     using Red = typename P::Red;
     constexpr int TR = L::TR, WT = L::WT, ST = L::ST;
     constexpr int XV = P::kChunkCols * P::kXElemBytes;                  // x bytes per vector per chunk
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + L::kAlign - 1) & ~uintptr_t(L::kAlign - 1));
-    const int CW = a.cons_warps, S = a.stages;
-    Red *red = reinterpret_cast<Red *>(smem + L::red_off(CW, S));
-    Red *part = reinterpret_cast<Red *>(smem + L::part_off(CW, S));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::bar_off(CW, S));
-    int *misc = reinterpret_cast<int *>(smem + L::misc_off(CW, S));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // align by offsetting the __shared__ array itself (not through an integer
+    // cast), so the compiler keeps every access in the shared address space
+    const uint32_t raw = smem_u32(smem_raw);
+    uint8_t *smem = smem_raw + (((raw + L::kAlign - 1) & ~uint32_t(L::kAlign - 1)) - raw);
+    const int S = a.stages;
+    Red *red = reinterpret_cast<Red *>(smem + L::red_off(S));
+    Red *part = reinterpret_cast<Red *>(smem + L::part_off(S));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off(S));
+    uint64_t *empty = full + S;
+    uint64_t *gather_bar = empty + S;           // K split: the leader CTA counts the others' partials
+    int *misc = reinterpret_cast<int *>(smem + L::misc_off(S));
     volatile int *abort_flag = misc;
     const MoeTables mt{misc + 4, misc + 4 + kMaxPairs, misc + 4 + 2 * kMaxPairs,
                        misc + 4 + 3 * kMaxPairs, misc + 1};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nthreads = blockDim.x;
+    constexpr int CW = kConsWarps;                  // S % CW == 0 (see make_plan)
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2 * CW * S; ++i) mbar_init(smem_u32(&bars[i]), 1);
+        for (int i = 0; i < S; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), 1);
+        }
+        mbar_init(smem_u32(gather_bar), (uint32_t)max(a.ksplit - 1, 1));
         *abort_flag = 0;
         fence_mbar_init();
     }
+    griddep_launch_dependents();
     if constexpr (MOE) {
+        // ids may come from the previous kernel (a router): wait for it first
+        griddep_wait();
         // Group the (token, slot) pairs by expert; every CTA derives the same table.
         const int P_ = a.n_vec * a.n_active;
         for (int p = threadIdx.x; p < P_; p += nthreads) {
@@ -433,6 +493,8 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
 
     const int n_work = MOE ? (*mt.n_groups) * a.num_tiles : a.num_tiles;
     const bool split = a.ksplit > 1;
+    // every CTA of the cluster has initialised its barriers before any remote access
+    if (split) cluster_arrive_relaxed();
     const int rank = split ? (int)cluster_ctarank() : 0;
     const int work0 = split ? (int)(blockIdx.x / a.ksplit) : (int)blockIdx.x;
     const int wstep = split ? max(n_work, 1) : (int)gridDim.x;     // split: one tile per cluster
@@ -447,10 +509,22 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
             const uint64_t polX = l2_evict_last_policy();
             prefetch_tensormap(&a.tmW);
             if (!MOE) prefetch_tensormap(&a.tmX);
-            // Warp w consumes local chunks j = w, w+CW, ... of every work item, so
-            // its n-th stage fill is chunk j of item t with n = t*cnt(w) + j/CW.
-            int items = 0;
-            for (int work = work0; work < n_work; work += wstep, ++items) {
+            // The weights never depend on the previous kernel: the first S stages'
+            // weight tiles are requested at once, and only then does the producer
+            // wait for the previous kernel (x and the expert ids may come from it).
+            uint32_t n_pre = 0;
+            if (!MOE) {
+                for (int work = work0; work < n_work && n_pre < (uint32_t)S; work += wstep)
+                    for (int j = 0; j < nloc && n_pre < (uint32_t)S; ++j, ++n_pre) {
+                        const uint32_t fb = smem_u32(&full[n_pre]);
+                        mbar_arrive_expect_tx(fb, WT + NV * XV);
+                        tma_load_2d(smem_u32(smem + (size_t)n_pre * ST), &a.tmW, (k0 + j) * P::kBoxInner,
+                                    (int)((long long)(work % a.num_tiles) * TR), fb, polW);
+                    }
+                griddep_wait();
+            }
+            uint32_t n = 0;
+            for (int work = work0; work < n_work; work += wstep) {
                 const int tile = work % a.num_tiles;
                 int m = NV, g = 0;
                 long long row0 = (long long)tile * TR;
@@ -459,48 +533,45 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                     m = mt.gsize[g];
                     row0 += (long long)mt.gexpert[g] * a.rows;
                 }
-                for (int j = 0; j < nloc; ++j) {
-                    const int w = j % CW;
-                    const uint32_t cnt = (uint32_t)((nloc - w + CW - 1) / CW);
-                    const uint32_t n = (uint32_t)items * cnt + (uint32_t)(j / CW);
+                for (int j = 0; j < nloc; ++j, ++n) {
                     const int s = n % S;
-                    const uint32_t full = smem_u32(&bars[w * S + s]);
-                    const uint32_t empty = smem_u32(&bars[CW * S + w * S + s]);
-                    if (n >= (uint32_t)S) mbar_wait(empty, ((n / S) - 1) & 1, abort_flag, a.fault);
-                    uint8_t *st = smem + (size_t)(w * S + s) * ST;
+                    uint8_t *st = smem + (size_t)s * ST;
+                    const uint32_t fb = smem_u32(&full[s]);
                     const int kc = k0 + j;
-                    mbar_arrive_expect_tx(full, WT + m * XV);
-                    tma_load_2d(smem_u32(st), &a.tmW, kc * P::kBoxInner, (int)row0, full, polW);
+                    if (n >= n_pre) {
+                        if (n >= (uint32_t)S) mbar_wait(smem_u32(&empty[s]), ((n / S) - 1) & 1, abort_flag, a.fault);
+                        mbar_arrive_expect_tx(fb, WT + m * XV);
+                        tma_load_2d(smem_u32(st), &a.tmW, kc * P::kBoxInner, (int)row0, fb, polW);
+                    }
                     if (!MOE) {
-                        tma_load_2d(smem_u32(st + WT), &a.tmX, kc * P::kChunkCols, 0, full, polX);
+                        tma_load_2d(smem_u32(st + WT), &a.tmX, kc * P::kChunkCols, 0, fb, polX);
                     } else {
                         for (int i = 0; i < m; ++i) {
                             const int p = mt.sorted[mt.gstart[g] + i];
                             const long long xr = a.x_per_slot ? p : p / a.n_active;
                             bulk_load(smem_u32(st + WT + i * XV),
-                                      a.x + xr * a.cols + (long long)kc * P::kChunkCols, XV, full, polX);
+                                      a.x + xr * a.cols + (long long)kc * P::kChunkCols, XV, fb, polX);
                         }
                     }
                 }
             }
             // no copy may still be landing in shared memory when the CTA exits
-            for (int w = 0; w < CW; ++w) {
-                const uint32_t total = (uint32_t)items * (uint32_t)((nloc - w + CW - 1) / CW);
-                for (int s = 0; s < S; ++s) {
-                    if (total <= (uint32_t)s) continue;
-                    const uint32_t last = total - 1 - ((total - 1 - s) % S);   // last fill of stage s
-                    const uint32_t bar = smem_u32(&bars[w * S + s]);
-                    const unsigned long long t0 = globaltimer();
-                    while (!mbar_try_wait(bar, (last / S) & 1))
-                        if (globaltimer() - t0 > kWaitTimeoutNs) break;
-                }
+            for (int s = 0; s < S; ++s) {
+                if (n <= (uint32_t)s) continue;
+                const uint32_t last = n - 1 - ((n - 1 - s) % S);             // last fill of stage s
+                const uint32_t bar = smem_u32(&full[s]);
+                const long long t0 = sm_cycles();
+                while (!mbar_try_wait(bar, (last / S) & 1))
+                    if (sm_cycles() - t0 > kWaitTimeoutCycles) break;
             }
         }
         __syncwarp();
     } else {
         // ---------------- consumers
-        uint32_t seq = 0;
-        for (int work = work0; work < n_work; work += wstep) {
+        if (split) cluster_wait();               // the leader's gather buffer and barrier exist
+        griddep_wait();                          // y may still be in use by the previous kernel
+        uint32_t base = 0;                       // fill number of the current item's first chunk
+        for (int work = work0; work < n_work; work += wstep, base += nloc) {
             const int tile = work % a.num_tiles;
             int m = NV, g = 0;
             if (MOE) { g = work / a.num_tiles; m = mt.gsize[g]; }
@@ -509,13 +580,16 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
             for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int v = 0; v < NV; ++v) acc[r][v] = zero_acc<Acc>();
-            for (int j = warp; j < nloc; j += CW) {
-                const uint32_t n = seq++;
+            // fill n lands in stage n % S and belongs to warp n % CW (S is a multiple
+            // of CW): each stage is only ever consumed by one warp, in fill order,
+            // so a wait can never mistake a stage's previous phase for its next
+            for (int j = (warp - (int)(base % CW) + CW) % CW; j < nloc; j += CW) {
+                const uint32_t n = base + j;
                 const int s = n % S;
-                mbar_wait(smem_u32(&bars[warp * S + s]), (n / S) & 1, abort_flag, a.fault);
-                const uint8_t *st = smem + (size_t)(warp * S + s) * ST;
+                mbar_wait(smem_u32(&full[s]), (n / S) & 1, abort_flag, a.fault);
+                const uint8_t *st = smem + (size_t)s * ST;
                 if constexpr (!MOE) {
-                    P::template consume<NV, R>(st, st + WT, lane, acc);
+                    consume_chunk<P, NV, R>(st, st + WT, lane, acc);
                 } else {
                     // only the group's m vectors are multiplied
                     switch (m) {
@@ -525,7 +599,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
             Acc acc_m[R][M_];                                                        \
             _Pragma("unroll") for (int r = 0; r < R; ++r)                            \
                 _Pragma("unroll") for (int v = 0; v < M_; ++v) acc_m[r][v] = acc[r][v]; \
-            P::template consume<M_, R>(st, st + WT, lane, acc_m);                    \
+            consume_chunk<P, M_, R>(st, st + WT, lane, acc_m);                       \
             _Pragma("unroll") for (int r = 0; r < R; ++r)                            \
                 _Pragma("unroll") for (int v = 0; v < M_; ++v) acc[r][v] = acc_m[r][v]; \
         }                                                                            \
@@ -537,9 +611,9 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                     }
                 }
                 __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&bars[CW * S + warp * S + s]));
+                if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
             }
-            // cross-warp reduction of the tile, in fixed warp order
+            // reduction of the tile over all consumer warps, in fixed warp order
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
@@ -548,42 +622,43 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
             named_barrier(1, CW * 32);
             for (int e = threadIdx.x; e < TR * m; e += CW * 32) {
                 const int v = e / TR, rr = e % TR;
-                Red sum = 0;
-                for (int w2 = 0; w2 < CW; ++w2) sum += red[(w2 * NV + v) * TR + rr];
+                Red sum = red[v * TR + rr];
+                for (int w2 = 1; w2 < CW; ++w2) sum += red[(w2 * NV + v) * TR + rr];
                 const long long row = (long long)tile * TR + rr;
-                if (split) part[v * TR + rr] = sum;
-                else if (row < a.rows) store_out<P, MOE>(a, mt, g, v, row, sum);
+                if (split) {
+                    // this CTA's partial goes to slot `rank` of the leader's gather buffer
+                    const uint32_t slot = smem_u32(&part[((size_t)rank * NV + v) * TR + rr]);
+                    if constexpr (std::is_same<Red, int>::value) st_shared_cluster_s32(map_shared_rank(slot, 0), sum);
+                    else st_shared_cluster_f32(map_shared_rank(slot, 0), sum);
+                } else if (row < a.rows) {
+                    store_out<P, MOE>(a, mt, g, v, row, sum);
+                }
             }
             named_barrier(1, CW * 32);
+            if (split && rank != 0 && threadIdx.x == 0)
+                mbar_arrive_remote(map_shared_rank(smem_u32(gather_bar), 0));
         }
     }
 
     if (split) {
-        // K was split across the cluster: CTA `rank` combines its share of the
-        // tile's outputs over all ranks' partials, in rank order, through DSMEM.
-        cluster_sync();
+        // K was split across the cluster: the leader (rank 0) adds the ranks'
+        // partials in rank order and stores the tile; the other CTAs are done.
+        if (warp == CW) cluster_wait();          // the producer warp completes the cluster barrier too
+        __syncthreads();                         // the leader's own partial is in `part` for all threads
         const int work = work0;
-        if (work < n_work) {
+        if (rank == 0 && work < n_work) {
+            if (a.ksplit > 1) mbar_wait_cluster(smem_u32(gather_bar), 0, abort_flag, a.fault);
             const int tile = work % a.num_tiles;
             int m = NV, g = 0;
             if (MOE) { g = work / a.num_tiles; m = mt.gsize[g]; }
-            const int E = TR * m;
-            const int e0 = (int)((long long)rank * E / a.ksplit);
-            const int e1 = (int)((long long)(rank + 1) * E / a.ksplit);
-            for (int e = e0 + threadIdx.x; e < e1; e += nthreads) {
+            for (int e = threadIdx.x; e < TR * m; e += nthreads) {
                 const int v = e / TR, rr = e % TR;
-                const uint32_t addr = smem_u32(&part[v * TR + rr]);
-                Red sum = 0;
-                for (int q = 0; q < a.ksplit; ++q) {
-                    const uint32_t ra = map_shared_rank(addr, q);
-                    if constexpr (std::is_same<Red, int>::value) sum += ld_shared_cluster_s32(ra);
-                    else sum += ld_shared_cluster_f32(ra);
-                }
+                Red sum = part[(size_t)v * TR + rr];
+                for (int q = 1; q < a.ksplit; ++q) sum += part[((size_t)q * NV + v) * TR + rr];
                 const long long row = (long long)tile * TR + rr;
                 if (row < a.rows) store_out<P, MOE>(a, mt, g, v, row, sum);
             }
         }
-        cluster_sync();
     }
 }
 
@@ -671,7 +746,7 @@ __global__ void requant_debug_kernel(const int32_t *__restrict__ acc, const int3
 namespace {
 
 struct Plan {
-    int cons_warps = 4, stages = 2, ksplit = 1, grid = 1;
+    int stages = 4, ksplit = 1, grid = 1;
     size_t smem = 0;
 };
 
@@ -692,31 +767,57 @@ hq_status encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, ui
     return HQ_OK;
 }
 
-// Launch geometry.  Row tiles are 32*R rows; when there are too few tiles to
-// give every SM work, K is split across a cluster of up to 8 CTAs.
-template <class P, int NV, int R>
-Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks) {
-    using L = Layout<P, NV, R>;
+// Ring depth choice, overridable for tuning: HQ_STAGES_PER_WARP=2 gives every
+// consumer warp a double buffer (8 stages, fewer CTAs per SM).
+bool prefer_double_buffer() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("HQ_STAGES_PER_WARP");
+        v = (e && atoi(e) == 2) ? 1 : 0;
+    }
+    return v == 1;
+}
+
+// Launch geometry: ctas_per_sm<NV,R>() CTAs per SM, the stage ring sized to
+// share the SM's shared memory among them.  Row tiles are 32*R rows; when
+// there are too few to fill every CTA slot, K is split across a cluster of up
+// to 8 CTAs, never beyond one wave.
+template <class P, int NV, int R, bool MOE>
+Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_per_thread) {
+    using L = Layout<P, NV, R, MOE>;
     Plan p;
-    const long long target = 2LL * dev.num_sms;          // CTAs wanted in flight
-    int ks = 1;
-    while (ks < 8 && n_work * ks < target && n_chunks >= 2 * ks) ks *= 2;
-    p.ksplit = ks;
-    const int chunks_per_cta = (n_chunks + ks - 1) / ks;
-    p.cons_warps = std::max(1, std::min(ks == 1 ? 4 : kMaxConsWarps, chunks_per_cta));
-    const int per_warp = (chunks_per_cta + p.cons_warps - 1) / p.cons_warps;
-    p.stages = (ks == 1) ? 4 : std::max(1, std::min(2, per_warp));
     const size_t budget = (size_t)dev.max_smem_optin;
-    while (p.stages > 1 && L::total(p.cons_warps, p.stages) > budget / 2) --p.stages;
-    while (p.cons_warps > 1 && L::total(p.cons_warps, p.stages) > budget) --p.cons_warps;
-    p.smem = L::total(p.cons_warps, p.stages);
+    const int want = ctas_per_sm<NV, R>();
+    // two stages per consumer warp (a double buffer each), more when room allows
+    p.stages = 2 * kConsWarps;
+    while (L::total(p.stages + kConsWarps) * want <= budget && p.stages < 4 * kConsWarps) p.stages += kConsWarps;
+    p.smem = L::total(p.stages);
+    const int regs = std::max(32, regs_per_thread);
+    const long long by_regs = 65536 / (32 * (kConsWarps + 1) * ((regs + 7) / 8 * 8));
+    const long long per_sm = std::max<long long>(1, std::min<long long>({by_regs, (long long)want,
+                                                                          (long long)(budget / p.smem)}));
+    const long long slots = (long long)dev.num_sms * per_sm;
+    int ks = 1;
+    while (ks < 8 && n_work * ks * 2 <= slots && n_chunks >= 2 * ks) ks *= 2;
+    p.ksplit = ks;
     if (ks == 1) {
-        const long long per_sm = std::max<long long>(1, std::min<long long>(2, (long long)(budget / p.smem)));
-        p.grid = (int)std::min<long long>(n_work, (long long)dev.num_sms * per_sm);
+        // the same number of tiles for every CTA: with HBM shared fairly, CTAs then finish together
+        const long long per_cta = (n_work + slots - 1) / slots;
+        p.grid = (int)((n_work + per_cta - 1) / per_cta);
     } else {
         p.grid = (int)(n_work * ks);
     }
     return p;
+}
+
+template <class P, int NV, int R, bool MOE>
+int kernel_regs() {
+    static int regs = -1;
+    if (regs < 0) {
+        cudaFuncAttributes fa;
+        regs = (cudaFuncGetAttributes(&fa, matvec_tma_kernel<P, NV, R, MOE>) == cudaSuccess) ? fa.numRegs : 128;
+    }
+    return regs;
 }
 
 size_t dev_smem_limit() {
@@ -733,32 +834,39 @@ hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
     int devi = 0;
     cudaGetDevice(&devi);
     cudaError_t e = cudaSuccess;
-    if (devi < 0 || devi >= 64 || configured[devi] < (int)p.smem) {
+    if (devi < 0 || devi >= 64 || configured[devi] == 0) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev_smem_limit());
         if (e == cudaSuccess)
             e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        // one shared-memory carveout for every launch: consecutive matvecs of
+        // different sizes then never make an SM reconfigure its L1/shared split
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
         if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "cudaFuncSetAttribute: %s", cudaGetErrorString(e));
-        if (devi >= 0 && devi < 64) configured[devi] = (int)dev_smem_limit();
+        if (devi >= 0 && devi < 64) configured[devi] = 1;
     }
-    a.cons_warps = p.cons_warps;
     a.stages = p.stages;
     a.ksplit = p.ksplit;
     if (p.grid <= 0) return HQ_OK;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
-    cfg.blockDim = dim3((unsigned)(32 * (p.cons_warps + 1)), 1, 1);
+    cfg.blockDim = dim3((unsigned)(32 * (kConsWarps + 1)), 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    cfg.numAttrs = 0;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
     if (p.ksplit > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)p.ksplit;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = (unsigned)p.ksplit;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
     }
+    cfg.attrs = attr;
+    cfg.numAttrs = na;
     e = cudaLaunchKernelEx(&cfg, kern, a);
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "matvec launch: %s", cudaGetErrorString(e));
     return HQ_OK;
@@ -800,7 +908,7 @@ hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y,
     a.n_chunks = (int)(cols / P::kChunkCols);
     a.num_tiles = (int)((rows + 32 * R - 1) / (32 * R));
     a.n_vec = NV;
-    const Plan p = make_plan<P, NV, R>(dev, a.num_tiles, a.n_chunks);
+    const Plan p = make_plan<P, NV, R, false>(dev, a.num_tiles, a.n_chunks, kernel_regs<P, NV, R, false>());
     return launch_tma<P, NV, R, false>(a, p, stream);
 }
 
@@ -848,7 +956,8 @@ hq_status moe_nv(const DeviceInfo &dev, const void *W_bank, const int32_t *ids, 
     // pairs can form (every pair its own expert, at most n_experts of them).
     const long long max_groups = std::min<long long>((long long)n_vec * n_active,
                                                      n_experts * (((long long)n_vec * n_active + NVMAX - 1) / NVMAX));
-    Plan p = make_plan<P, NVMAX, R>(dev, (long long)a.num_tiles * max_groups, a.n_chunks);
+    Plan p = make_plan<P, NVMAX, R, true>(dev, (long long)a.num_tiles * max_groups, a.n_chunks,
+                                          kernel_regs<P, NVMAX, R, true>());
     if (p.ksplit > 1) p.grid = (int)((long long)a.num_tiles * max_groups * p.ksplit);
     return launch_tma<P, NVMAX, R, true>(a, p, stream);
 }

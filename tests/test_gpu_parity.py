@@ -28,6 +28,15 @@ def hq():
     assert hq.hq_device_fault() == 0
 
 
+@pytest.fixture(autouse=True)
+def no_device_fault(request, hq):
+    """Every test leaves the device fault word clear (the invalid-id test clears
+    the bit it expects itself): no bounded wait may ever time out."""
+    yield
+    f = hq.hq_device_fault()
+    assert f == 0, f"{request.node.name} left device fault word {f:#x}: {hq.hq_last_error()}"
+
+
 def dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
@@ -197,6 +206,8 @@ def test_full_size_lm_heads_sampled(hq):
             blocks[r0:r1] = oracle.quantize_q8_0(synthetic.weights(g, r1 - r0, cols))
         x = synthetic.activations(g, 1, cols)
         y = gpu_matvec(hq, "q8_0", blocks, x, rows, cols)
+        f = hq.hq_device_fault()
+        assert f == 0, f"{rows}x{cols}: fault word {f:#x} ({hq.hq_last_error()})"
         for lo, hi in _sampled_rows(rows, n=40):
             y_ref, T = oracle.matvec_rows("q8_0", blocks, x, rows, cols, lo, hi)
             assert_within(y[:, lo:hi], y_ref, T, f"lm_head {rows}x{cols} rows {lo}:{hi}")
