@@ -40,10 +40,14 @@ import numpy as np  # noqa: E402
 
 from quantized_weight_matvec_hq_gb300 import synthetic  # noqa: E402
 
+# name -> (model shape, format, q|k|v and gate|up row-fused)
 WORKLOADS = {
-    "8b-q8_0": ("8b-dense", "q8_0"),
-    "8b-q4_0": ("8b-dense", "q4_0"),
-    "qwen3-0.6b-q8_0": ("qwen3-0.6b", "q8_0"),
+    "8b-q8_0": ("8b-dense", "q8_0", True),
+    "8b-q8_0-unfused": ("8b-dense", "q8_0", False),
+    "8b-q4_0": ("8b-dense", "q4_0", True),
+    "8b-q4_0-unfused": ("8b-dense", "q4_0", False),
+    "qwen3-0.6b-q8_0": ("qwen3-0.6b", "q8_0", True),
+    "qwen3-0.6b-q8_0-unfused": ("qwen3-0.6b", "q8_0", False),
 }
 
 
@@ -56,8 +60,8 @@ def workload_matrices(name, shape=None, fmt=None):
         one = weight_bytes(fmt, rows, cols)
         copies = max(4, -(-520_000_000 // one))
         return f"single {rows}x{cols}", fmt, [(f"m{rows}x{cols}", rows, cols)] * copies
-    model, fmt = WORKLOADS[name]
-    return model, fmt, synthetic.decode_token_shapes(model)
+    model, fmt, fused = WORKLOADS[name]
+    return model, fmt, synthetic.decode_token_shapes(model, fused)
 
 
 def weight_bytes(fmt, rows, cols):
@@ -134,6 +138,41 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def dist_env():
+    """(world size, rank, local rank) from the torchrun environment."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(values, device):
+    """Element-wise max of per-rank timings (the slowest replica sets the step
+    time); needs an initialised process group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def aggregate_value(world, bytes_per_step, ms_per_step):
+    """Whole-job weight GB/s: every replica streams bytes_per_step per step."""
+    return world * bytes_per_step / (ms_per_step / 1e3) / 1e9
+
+
+def read_traffic(path, workload, n_vec, shape):
+    """DRAM bytes (read + write) per step of the matvec kernel, from a line
+    `<workload> n_vec=<k> dram_bytes_per_step=<int>` of the ncu summary file;
+    None when the file has no line for this configuration."""
+    if shape or not os.path.exists(path):
+        return None
+    for ln in open(path):
+        parts = ln.split()
+        if len(parts) >= 3 and parts[0] == workload and parts[1] == f"n_vec={n_vec}" \
+                and parts[2].startswith("dram_bytes_per_step="):
+            return int(parts[2].split("=", 1)[1])
+    return None
+
+
 # ----------------------------------------------------------------- CUDA helpers
 
 def _cudart():
@@ -168,19 +207,30 @@ class Step:
             raise RuntimeError(f"workload needs {total / 1e9:.1f} GB, only {free / 1e9:.1f} GB free")
         self.W, self.x, self.y = [], [], []
         quant = hq.hq_quantize_q8_0 if self.fmt == "q8_0" else hq.hq_quantize_q4_0
+        # every matvec's x and y live in one contiguous buffer each (16-byte
+        # aligned views), so a step's inputs and outputs cross PCIe/C2C in one copy
+        xo, yo = [], []
+        nx = ny = 0
         for (_, rows, cols) in self.shapes:
+            xo.append(nx)
+            yo.append(ny)
+            nx += -(-n_vec * cols // 4) * 4
+            ny += -(-n_vec * rows // 4) * 4
+        self.x_all = torch.randn(nx, generator=g, device=device, dtype=torch.float32)
+        self.y_all = torch.empty(ny, device=device, dtype=torch.float32)
+        for i, (_, rows, cols) in enumerate(self.shapes):
             wf = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32).mul_(0.02)
             wq = torch.empty((rows, weight_bytes(self.fmt, 1, cols)), dtype=torch.uint8, device=device)
             quant(wf, wq, rows, cols)
             del wf
             self.W.append(wq)
-            self.x.append(torch.randn((n_vec, cols), generator=g, device=device, dtype=torch.float32))
-            self.y.append(torch.empty((n_vec, rows), dtype=torch.float32, device=device))
+            self.x.append(self.x_all[xo[i]:xo[i] + n_vec * cols].view(n_vec, cols))
+            self.y.append(self.y_all[yo[i]:yo[i] + n_vec * rows].view(n_vec, rows))
         torch.cuda.synchronize()
         self.fn = hq.hq_matvec_q8_0 if self.fmt == "q8_0" else hq.hq_matvec_q4_0
         self.weight_bytes = sum(weight_bytes(self.fmt, r, c) for (_, r, c) in self.shapes)
-        self.x_bytes = sum(4 * n_vec * c for (_, r, c) in self.shapes)
-        self.y_bytes = sum(4 * n_vec * r for (_, r, c) in self.shapes)
+        self.x_bytes = int(self.x_all.numel()) * 4
+        self.y_bytes = int(self.y_all.numel()) * 4
 
     def launch_all(self, stream, events=None):
         for i, (_, rows, cols) in enumerate(self.shapes):
@@ -307,16 +357,16 @@ def main():
     ap.add_argument("--format", choices=["q8_0", "q4_0"], default="q8_0", help="format for --shape")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--traffic-file", default=os.path.join(ROOT, "profiles", "traffic.json"),
-                    help="per-launch DRAM bytes of the matvec kernel from an ncu capture")
+    ap.add_argument("--traffic-file", default=os.path.join(ROOT, "profiles", "dram_traffic.txt"),
+                    help="DRAM bytes per step of the matvec kernel, from an ncu capture (text)")
     args = ap.parse_args()
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local_rank = dist_env()
     model, fmt, shapes = workload_matrices(args.workload, args.shape, args.format)
+    fused_note = (" with q|k|v and gate|up row-fused (same input)" if WORKLOADS[args.workload][2]
+                  else ", every projection its own call")
     config = {"workload": (f"{model} decode token, {fmt}, n_vec={args.n_vec}: "
-                           f"{len(shapes)} matvecs (all projections + lm_head)") if not args.shape else
+                           f"{len(shapes)} matvecs (all projections + lm_head){fused_note}") if not args.shape else
                           (f"{len(shapes)} distinct {args.shape} {fmt} matrices per step, n_vec={args.n_vec}"),
               "model_shape": model, "format": fmt, "n_vec": args.n_vec, "matvecs_per_step": len(shapes),
               "l2": "inputs larger than L2 (all weights distinct, 7.97 GB Q8_0 / 4.2 GB Q4_0 per step)"
@@ -384,52 +434,42 @@ def main():
             per_launch += np.array(events.durations_ms())
         per_launch /= args.steps
         # ---- end to end: pinned host x in, y out, every step
-        x_host = [t.cpu().pin_memory() for t in step.x]
-        y_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in step.y]
-        s = torch.cuda.current_stream()
+        x_host = step.x_all.cpu().pin_memory()
+        y_host = torch.empty(step.y_all.shape, dtype=torch.float32).pin_memory()
         for _ in range(2):
-            for xd, xh in zip(step.x, x_host):
-                xd.copy_(xh, non_blocking=True)
+            step.x_all.copy_(x_host, non_blocking=True)
             graph.replay()
-            for yd, yh in zip(step.y, y_host):
-                yh.copy_(yd, non_blocking=True)
+            y_host.copy_(step.y_all, non_blocking=True)
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(args.steps):
-            for xd, xh in zip(step.x, x_host):
-                xd.copy_(xh, non_blocking=True)
+            step.x_all.copy_(x_host, non_blocking=True)
             graph.replay()
-            for yd, yh in zip(step.y, y_host):
-                yh.copy_(yd, non_blocking=True)
+            y_host.copy_(step.y_all, non_blocking=True)
         e1.record()
         e1.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.steps
     clk = clocks.summary()
 
     if world > 1:
-        t = torch.tensor([dev_ms, e2e_ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dev_ms, e2e_ms = float(t[0]), float(t[1])
+        dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_ms], device)
 
     if rank != 0:
         torch.distributed.destroy_process_group()
         return
 
     peak, peak_kind = load_peaks()
-    value = world * step.weight_bytes / (dev_ms / 1e3) / 1e9
-    e2e = world * step.weight_bytes / (e2e_ms / 1e3) / 1e9
+    value = aggregate_value(world, step.weight_bytes, dev_ms)
+    e2e = aggregate_value(world, step.weight_bytes, e2e_ms)
+    # Roofline of the matvec kernel: the step consists of its launches only, so
+    # the mean launch duration is the step's device time over the launch count.
+    # The event pairs of the per-shape breakdown add a few microseconds per
+    # launch and break the programmatic-launch overlap: a breakdown only.
     alg = np.array([weight_bytes(fmt, r, c) + 4 * args.n_vec * (r + c) for (_, r, c) in shapes], dtype=np.float64)
+    achieved = float(alg.sum() / (dev_ms / 1e3) / 1e9)
+    traffic = read_traffic(args.traffic_file, args.workload, args.n_vec, args.shape)
     kernel_ms = float(per_launch.sum())
-    achieved = float(alg.sum() / (kernel_ms / 1e3) / 1e9)
-    traffic = None
-    if os.path.exists(args.traffic_file):
-        try:
-            tr = json.load(open(args.traffic_file))
-            if tr.get("workload") == args.workload and tr.get("n_vec") == args.n_vec:
-                traffic = tr.get("dram_bytes_per_launch")
-        except (OSError, ValueError):
-            traffic = None
     by_shape = {}
     for (nm, r, c), ms, b in zip(shapes, per_launch, alg):
         k = f"{nm} {r}x{c}"
@@ -438,7 +478,7 @@ def main():
         d[1] += b
         d[2] += 1
     shapes_out = {k: {"launches": v[2], "us_per_launch": round(v[0] / v[2] * 1e3, 3),
-                      "gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1), "frac": round(v[1] / (v[0] / 1e3) / 1e9 / peak, 4)}
+                      "gbs": round(v[1] / (v[0] / 1e3) / 1e9, 1)}
                   for k, v in by_shape.items()}
 
     line = {
@@ -449,12 +489,16 @@ def main():
         "tok_per_s": round(1e3 / dev_ms * world, 2),
         "frac_of_hbm": round(value / world / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
-                     "kernel": "matvec_tma_kernel (all launches of the step)",
-                     "algorithmic_bytes_per_step": int(alg.sum()),
-                     "kernel_ms_per_step": round(kernel_ms, 5)},
-        "per_shape": shapes_out,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": (round(traffic / len(shapes)) if traffic is not None else None),
+                     "traffic_unit": "DRAM bytes read+written per launch (mean over the step), from ncu",
+                     "algorithmic_bytes_per_launch": round(float(alg.sum()) / len(shapes)),
+                     "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs), burst",
+                     "kernel": "matvec_tma_kernel (every launch of the step)",
+                     "launches_per_step": len(shapes),
+                     "mean_launch_us": round(dev_ms * 1e3 / len(shapes), 3)},
+        "per_shape_event_pairs": shapes_out,
+        "per_shape_event_pairs_ms_per_step": round(kernel_ms, 4),
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": int(step.x_bytes), "d2h_bytes_per_step": int(step.y_bytes)},
         "gpu_launches": len(shapes) * args.steps,

@@ -70,10 +70,25 @@ def expert_ids(g: np.random.Generator, n_vec: int, n_active: int, n_experts: int
     return out
 
 
-def decode_token_shapes(model: str):
-    """The (name, rows, cols) list of one decode token's matvecs, lm_head last."""
+def fuse_same_input(layer):
+    """Row-concatenate the projections that read the same activation vector:
+    q|k|v (the attention input) and gate|up (the MLP input).  The weight bytes
+    are unchanged; a decode step then makes 4 matvec calls per layer, not 7."""
+    by = dict((n, (r, c)) for n, r, c in layer)
+    qkv = ("qkv", by["q"][0] + by["k"][0] + by["v"][0], by["q"][1])
+    gate_up = ("gate_up", by["gate"][0] + by["up"][0], by["gate"][1])
+    return (qkv, ("o",) + by["o"], gate_up, ("down",) + by["down"])
+
+
+def decode_token_shapes(model: str, fused: bool = False):
+    """The (name, rows, cols) list of one decode token's matvecs, lm_head last;
+    with fused=True, q|k|v and gate|up are single row-concatenated matvecs."""
     if model == "qwen3-0.6b":
-        return [s for _ in range(QWEN3_0_6B_LAYERS) for s in QWEN3_0_6B_LAYER] + [QWEN3_0_6B_LM_HEAD]
-    if model == "8b-dense":
-        return [s for _ in range(DENSE_8B_LAYERS) for s in DENSE_8B_LAYER] + [DENSE_8B_LM_HEAD]
-    raise ValueError(model)
+        layer, n, head = QWEN3_0_6B_LAYER, QWEN3_0_6B_LAYERS, QWEN3_0_6B_LM_HEAD
+    elif model == "8b-dense":
+        layer, n, head = DENSE_8B_LAYER, DENSE_8B_LAYERS, DENSE_8B_LM_HEAD
+    else:
+        raise ValueError(model)
+    if fused:
+        layer = fuse_same_input(layer)
+    return [s for _ in range(n) for s in layer] + [head]
