@@ -767,6 +767,16 @@ hq_status encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, ui
     return HQ_OK;
 }
 
+// Deeper rings when fewer CTAs share an SM (HQ_ADAPTIVE_RING=0 turns it off, for comparison).
+bool adaptive_ring() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("HQ_ADAPTIVE_RING");
+        v = (e && atoi(e) == 0) ? 0 : 1;
+    }
+    return v == 1;
+}
+
 // Ring depth choice, overridable for tuning: HQ_STAGES_PER_WARP=2 gives every
 // consumer warp a double buffer (8 stages, fewer CTAs per SM).
 bool prefer_double_buffer() {
@@ -806,6 +816,15 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
         p.grid = (int)((n_work + per_cta - 1) / per_cta);
     } else {
         p.grid = (int)(n_work * ks);
+    }
+    // the ring takes the shared memory the SM's resident CTAs leave: fewer CTAs
+    // per SM get deeper rings, so an SM keeps about the same bytes in flight
+    if (adaptive_ring()) {
+        const long long resident = std::max<long long>(1, (p.grid + dev.num_sms - 1) / dev.num_sms);
+        int st = p.stages;
+        while (st + kConsWarps <= 16 && L::total(st + kConsWarps) * resident <= budget) st += kConsWarps;
+        p.stages = st;
+        p.smem = L::total(st);
     }
     return p;
 }
