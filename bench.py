@@ -8,6 +8,13 @@ weight bytes, all distinct (7.97 GB > L2, so no flush is needed).  Weights are
 seeded synthetic N(0, 0.02) fp32, quantized on the GPU; each matvec gets its
 own x ~ N(0, 1).  The step is captured once as a CUDA graph and replayed.
 
+Other workloads (--workload): the same token unfused, in Q4_0, or Qwen3-0.6B-
+shaped; "moe-q8_0" -- 48 MoE layers, each an expert-indexed gate|up and down
+launch over its own bank of 128 experts (8 active per token, drawn per layer);
+"int8-requant" -- 96 distinct copies of each of the 1024x3072 and 3072x1024
+int8 matrices with per-row requant.  --n-vec sets the activation vectors per
+launch (1..8); for MoE the weight bytes count the distinct experts read.
+
 value      = weight bytes per step / device time per step (GB/s, 1e9 B),
              summed over ranks (replicas, weak scaling).
 e2e        = the same, with each step's x copied host->device from pinned
@@ -40,31 +47,85 @@ import numpy as np  # noqa: E402
 
 from quantized_weight_matvec_hq_gb300 import synthetic  # noqa: E402
 
-# name -> (model shape, format, q|k|v and gate|up row-fused)
+# name -> (kind, model shape, format, q|k|v and gate|up row-fused)
 WORKLOADS = {
-    "8b-q8_0": ("8b-dense", "q8_0", True),
-    "8b-q8_0-unfused": ("8b-dense", "q8_0", False),
-    "8b-q4_0": ("8b-dense", "q4_0", True),
-    "8b-q4_0-unfused": ("8b-dense", "q4_0", False),
-    "qwen3-0.6b-q8_0": ("qwen3-0.6b", "q8_0", True),
-    "qwen3-0.6b-q8_0-unfused": ("qwen3-0.6b", "q8_0", False),
+    "8b-q8_0": ("dense", "8b-dense", "q8_0", True),
+    "8b-q8_0-unfused": ("dense", "8b-dense", "q8_0", False),
+    "8b-q4_0": ("dense", "8b-dense", "q4_0", True),
+    "8b-q4_0-unfused": ("dense", "8b-dense", "q4_0", False),
+    "qwen3-0.6b-q8_0": ("dense", "qwen3-0.6b", "q8_0", True),
+    "qwen3-0.6b-q8_0-unfused": ("dense", "qwen3-0.6b", "q8_0", False),
+    "moe-q8_0": ("moe", "moe-128x8-hidden2048", "q8_0", True),
+    "int8-requant": ("int8", "int8-1024x3072+3072x1024", "i8", False),
 }
+# MoE decode: a stack of this many layers, each with its own bank of experts
+# (128 x (gate|up 1536x2048 + down 2048x768) Q8_0 = 642 MB per layer)
+MOE_LAYERS = 48
+# int8 GEMV: this many distinct copies of each of the two matrices per step (604 MB)
+INT8_COPIES = 96
 
 
-def workload_matrices(name, shape=None, fmt=None):
-    """(model, format, [(name, rows, cols), ...]) of one step.  With `shape`
-    ("ROWSxCOLS"), the step is enough distinct copies of that one matrix to
-    exceed 4x the L2 (>= 520 MB) so that no launch reads from L2."""
+class Op:
+    """One launch of a step: a dense matvec, an expert-indexed MoE matvec or an
+    int8 requant GEMV, with the bytes it reads and writes."""
+
+    def __init__(self, kind, name, rows, cols, fmt, n_experts=0, n_active=0, x_per_slot=0, ids=None):
+        self.kind, self.name, self.rows, self.cols, self.fmt = kind, name, rows, cols, fmt
+        self.n_experts, self.n_active, self.x_per_slot, self.ids = n_experts, n_active, x_per_slot, ids
+
+    def x_elems(self, n_vec):
+        return n_vec * (self.n_active if self.x_per_slot else 1) * self.cols
+
+    def y_elems(self, n_vec):
+        return n_vec * (self.n_active if self.kind == "moe" else 1) * self.rows
+
+    def weight_bytes(self):
+        """Weight bytes one launch reads: for MoE, the distinct experts of the routing."""
+        if self.kind == "int8":
+            return self.rows * self.cols + 8 * self.rows               # + mult, shift
+        one = weight_bytes(self.fmt, self.rows, self.cols)
+        if self.kind == "moe":
+            return one * len(np.unique(self.ids))
+        return one
+
+    def alg_bytes(self, n_vec):
+        """Algorithmic bytes of a launch: weights read + x read + y written (+ expert ids)."""
+        el = 1 if self.kind == "int8" else 4
+        extra = self.ids.size * 4 if self.kind == "moe" else 0
+        return self.weight_bytes() + el * (self.x_elems(n_vec) + self.y_elems(n_vec)) + extra
+
+
+def workload_ops(name, n_vec, shape=None, fmt=None, seed=synthetic.SEED_BASE + 2):
+    """(model, format, [Op, ...]) of one step.  With `shape` ("ROWSxCOLS"), the
+    step is enough distinct copies of that one matrix to exceed 4x the L2
+    (>= 520 MB) so that no launch reads from L2."""
     if shape:
         rows, cols = (int(v) for v in shape.lower().split("x"))
         one = weight_bytes(fmt, rows, cols)
         copies = max(4, -(-520_000_000 // one))
-        return f"single {rows}x{cols}", fmt, [(f"m{rows}x{cols}", rows, cols)] * copies
-    model, fmt, fused = WORKLOADS[name]
-    return model, fmt, synthetic.decode_token_shapes(model, fused)
+        return f"single {rows}x{cols}", fmt, [Op("dense", f"m{rows}x{cols}", rows, cols, fmt)] * copies
+    kind, model, fmt, fused = WORKLOADS[name]
+    if kind == "dense":
+        return model, fmt, [Op("dense", n, r, c, fmt) for (n, r, c) in synthetic.decode_token_shapes(model, fused)]
+    if kind == "moe":
+        g = synthetic.rng(seed + 7)
+        ops = []
+        E, A, H, F = synthetic.MOE_N_EXPERTS, synthetic.MOE_N_ACTIVE, synthetic.MOE_HIDDEN, synthetic.MOE_FFN
+        for layer in range(MOE_LAYERS):
+            ids = synthetic.expert_ids(g, n_vec, A, E)
+            ops.append(Op("moe", f"gate_up{layer}", 2 * F, H, fmt, E, A, 0, ids))
+            ops.append(Op("moe", f"down{layer}", H, F, fmt, E, A, 1, ids))
+        return model, fmt, ops
+    ops = []
+    for i in range(INT8_COPIES):
+        for (r, c) in synthetic.INT8_SHAPES:
+            ops.append(Op("int8", f"i8_{r}x{c}_{i}", r, c, fmt))
+    return model, fmt, ops
 
 
 def weight_bytes(fmt, rows, cols):
+    if fmt == "i8":
+        return rows * cols
     return rows * (cols // 32) * (34 if fmt == "q8_0" else 18)
 
 
@@ -189,54 +250,121 @@ def _cudart():
 
 
 class Step:
-    """One decode token's matvecs, resident in HBM, launched through the C ABI."""
+    """One step's launches, resident in HBM, launched through the C ABI.  Every
+    launch's x (and, for MoE, the expert ids) and y live in one contiguous
+    buffer each (16-byte aligned views), so a step's inputs and outputs cross
+    the host link in one copy each."""
 
     def __init__(self, name, n_vec, device, seed, shape=None, fmt=None):
         import torch
         import quantized_weight_matvec_hq_gb300 as hq
         self.hq = hq
         self.torch = torch
-        self.model, self.fmt, self.shapes = workload_matrices(name, shape, fmt)
+        self.model, self.fmt, self.ops = workload_ops(name, n_vec, shape, fmt)
         self.n_vec = n_vec
         self.device = device
         g = torch.Generator(device=device)
         g.manual_seed(seed)
-        total = sum(weight_bytes(self.fmt, r, c) for (_, r, c) in self.shapes)
+        total = sum(self._stored_bytes(op) for op in self.ops)
         free, _ = torch.cuda.mem_get_info(device)
         if total > 0.8 * free:
             raise RuntimeError(f"workload needs {total / 1e9:.1f} GB, only {free / 1e9:.1f} GB free")
-        self.W, self.x, self.y = [], [], []
-        quant = hq.hq_quantize_q8_0 if self.fmt == "q8_0" else hq.hq_quantize_q4_0
-        # every matvec's x and y live in one contiguous buffer each (16-byte
-        # aligned views), so a step's inputs and outputs cross PCIe/C2C in one copy
-        xo, yo = [], []
-        nx = ny = 0
-        for (_, rows, cols) in self.shapes:
+        xdt = torch.int8 if self.fmt == "i8" else torch.float32
+        xo, yo, io = [], [], []
+        nx = ny = ni = 0
+        for op in self.ops:
             xo.append(nx)
             yo.append(ny)
-            nx += -(-n_vec * cols // 4) * 4
-            ny += -(-n_vec * rows // 4) * 4
-        self.x_all = torch.randn(nx, generator=g, device=device, dtype=torch.float32)
-        self.y_all = torch.empty(ny, device=device, dtype=torch.float32)
-        for i, (_, rows, cols) in enumerate(self.shapes):
-            wf = torch.randn((rows, cols), generator=g, device=device, dtype=torch.float32).mul_(0.02)
-            wq = torch.empty((rows, weight_bytes(self.fmt, 1, cols)), dtype=torch.uint8, device=device)
-            quant(wf, wq, rows, cols)
-            del wf
-            self.W.append(wq)
-            self.x.append(self.x_all[xo[i]:xo[i] + n_vec * cols].view(n_vec, cols))
-            self.y.append(self.y_all[yo[i]:yo[i] + n_vec * rows].view(n_vec, rows))
+            io.append(ni)
+            nx += -(-op.x_elems(n_vec) // 16) * 16
+            ny += -(-op.y_elems(n_vec) // 16) * 16
+            ni += -(-(op.ids.size if op.kind == "moe" else 0) // 4) * 4
+        if self.fmt == "i8":
+            self.x_all = torch.randint(-127, 128, (nx,), generator=g, device=device, dtype=torch.int8)
+        else:
+            self.x_all = torch.randn(nx, generator=g, device=device, dtype=torch.float32)
+        self.y_all = torch.empty(ny, device=device, dtype=xdt)
+        self.ids_all = torch.zeros(max(ni, 4), device=device, dtype=torch.int32)
+        self.W, self.x, self.y, self.ids, self.mult, self.shift = [], [], [], [], [], []
+        for i, op in enumerate(self.ops):
+            self.x.append(self.x_all[xo[i]:xo[i] + op.x_elems(n_vec)])
+            self.y.append(self.y_all[yo[i]:yo[i] + op.y_elems(n_vec)])
+            if op.kind == "moe":
+                v = self.ids_all[io[i]:io[i] + op.ids.size]
+                v.copy_(torch.from_numpy(op.ids.reshape(-1)))
+                self.ids.append(v)
+            else:
+                self.ids.append(None)
+            self.W.append(self._weights(op, g))
+            if op.kind == "int8":
+                m, sh = self._requant(op, self.W[-1], self.x[-1])
+                self.mult.append(m)
+                self.shift.append(sh)
+            else:
+                self.mult.append(None)
+                self.shift.append(None)
         torch.cuda.synchronize()
-        self.fn = hq.hq_matvec_q8_0 if self.fmt == "q8_0" else hq.hq_matvec_q4_0
-        self.weight_bytes = sum(weight_bytes(self.fmt, r, c) for (_, r, c) in self.shapes)
-        self.x_bytes = int(self.x_all.numel()) * 4
-        self.y_bytes = int(self.y_all.numel()) * 4
+        self.weight_bytes = sum(op.weight_bytes() for op in self.ops)
+        self.alg_bytes = [op.alg_bytes(n_vec) for op in self.ops]
+        self.x_bytes = int(self.x_all.numel()) * self.x_all.element_size()
+        self.ids_bytes = int(ni) * 4
+        self.y_bytes = int(self.y_all.numel()) * self.y_all.element_size()
+
+    def _stored_bytes(self, op):
+        if op.kind == "moe":
+            return op.n_experts * weight_bytes(op.fmt, op.rows, op.cols)
+        return weight_bytes(op.fmt, op.rows, op.cols)
+
+    def _weights(self, op, g):
+        """Quantized weights of one launch: N(0, 0.02) fp32 quantized on the GPU."""
+        torch, hq = self.torch, self.hq
+        if op.kind == "int8":
+            wf = torch.randn((op.rows, op.cols), generator=g, device=self.device, dtype=torch.float32).mul_(0.02)
+            wq = torch.empty((op.rows, op.cols), dtype=torch.int8, device=self.device)
+            op_scale = torch.empty(op.rows, dtype=torch.float32, device=self.device)
+            hq.hq_quantize_i8_rows(wf, wq, op_scale, op.rows, op.cols)
+            self._last_scale = op_scale
+            return wq
+        quant = hq.hq_quantize_q8_0 if op.fmt == "q8_0" else hq.hq_quantize_q4_0
+        rb = weight_bytes(op.fmt, 1, op.cols)
+        n_mat = op.n_experts if op.kind == "moe" else 1
+        wq = torch.empty((n_mat * op.rows, rb), dtype=torch.uint8, device=self.device)
+        for e in range(n_mat):                      # one matrix (expert) at a time bounds the fp32 scratch
+            wf = torch.randn((op.rows, op.cols), generator=g, device=self.device, dtype=torch.float32).mul_(0.02)
+            quant(wf, wq[e * op.rows:(e + 1) * op.rows], op.rows, op.cols)
+            del wf
+        return wq
+
+    def _requant(self, op, wq, xq):
+        """Per-row (mult, shift) for M = s_w * s_x / s_out, with s_out the 99th
+        percentile of |y| / 127 (about 1 % of outputs saturate).  s_x is the
+        symmetric per-tensor scale of x ~ U{-127..127} taken as 1/127."""
+        torch, hq = self.torch, self.hq
+        s_w = self._last_scale.double()
+        s_x = 1.0 / 127.0
+        acc = xq.view(self.n_vec, op.cols).double() @ wq.double().t()
+        yf = acc * s_w[None, :] * s_x
+        s_out = float(torch.quantile(yf.abs().flatten().float(), 0.99)) / 127.0
+        M = (s_w * s_x / s_out).cpu().numpy().astype(np.float64)
+        mult = np.empty(op.rows, dtype=np.int32)
+        shift = np.empty(op.rows, dtype=np.int32)
+        hq.hq_requant_params(M, op.rows, mult, shift)
+        return torch.from_numpy(mult).to(self.device), torch.from_numpy(shift).to(self.device)
 
     def launch_all(self, stream, events=None):
-        for i, (_, rows, cols) in enumerate(self.shapes):
+        hq, n_vec = self.hq, self.n_vec
+        for i, op in enumerate(self.ops):
             if events is not None:
                 events.record_before(i, stream)
-            self.fn(self.W[i], self.x[i], self.y[i], rows, cols, self.n_vec, stream=stream)
+            if op.kind == "dense":
+                fn = hq.hq_matvec_q8_0 if op.fmt == "q8_0" else hq.hq_matvec_q4_0
+                fn(self.W[i], self.x[i], self.y[i], op.rows, op.cols, n_vec, stream=stream)
+            elif op.kind == "moe":
+                hq.hq_moe_matvec_q8_0(self.W[i], self.ids[i], self.x[i], op.x_per_slot, self.y[i],
+                                      op.n_experts, op.n_active, op.rows, op.cols, n_vec, stream=stream)
+            else:
+                hq.hq_matvec_i8_requant(self.W[i], self.x[i], self.mult[i], self.shift[i], self.y[i],
+                                        op.rows, op.cols, n_vec, stream=stream)
             if events is not None:
                 events.record_after(i, stream)
 
@@ -300,37 +428,67 @@ class LaunchEvents:
 # ----------------------------------------------------------------- CPU oracle timing
 
 class OracleSample:
-    """The C oracle (one thread) on a bounded sample of the workload: the first
-    rows (about 4M weights) of each distinct matrix shape of the token,
-    quantized by the oracle itself.  One pass = one matvec per shape."""
+    """The C oracle (one thread) on a bounded sample of the workload, quantized
+    by the oracle itself.  One pass = one call per distinct launch shape:
+    dense -- the first rows (about 4M weights) of the matrix; MoE -- the first
+    layer's routing over a bank of only its distinct experts, each cut to its
+    first rows (about 4M weights in all); int8 -- each of the two matrices
+    whole (3.1M weights each), with the oracle's own requant recipe."""
 
     def __init__(self, name, n_vec, seed=synthetic.SEED_BASE + 2):
         import oracle
         self.oracle = oracle
-        self.model, self.fmt, shapes = workload_matrices(name)
+        self.model, self.fmt, ops = workload_ops(name, n_vec)
         self.n_vec = n_vec
-        distinct = []
-        for s_ in shapes:
-            if (s_[1], s_[2]) not in [(d[1], d[2]) for d in distinct]:
-                distinct.append(s_)
+        self.kind = ops[0].kind
+        distinct, keys = [], set()
+        for op in ops:
+            k = (op.rows, op.cols, op.x_per_slot)
+            if k not in keys:
+                keys.add(k)
+                distinct.append(op)
         g = synthetic.rng(seed)
-        self.slabs = []
-        for (nm, rows, cols) in distinct:
-            r = min(rows, max(8, (1 << 22) // cols))
-            W = synthetic.weights(g, r, cols)
-            blocks = oracle.quantize_q8_0(W) if self.fmt == "q8_0" else oracle.quantize_q4_0(W)
-            self.slabs.append((nm, r, cols, blocks, synthetic.activations(g, n_vec, cols)))
-        self.pass_bytes = sum(weight_bytes(self.fmt, r, c) for (_, r, c, _, _) in self.slabs)
+        self.calls = []
+        self.pass_bytes = 0
+        for op in distinct:
+            if op.kind == "dense":
+                r = min(op.rows, max(8, (1 << 22) // op.cols))
+                W = synthetic.weights(g, r, op.cols)
+                blocks = oracle.quantize_q8_0(W) if self.fmt == "q8_0" else oracle.quantize_q4_0(W)
+                x = synthetic.activations(g, n_vec, op.cols)
+                self.calls.append(lambda b=blocks, x=x, r=r, c=op.cols: oracle.matvec(self.fmt, b, x, r, c))
+                self.pass_bytes += weight_bytes(self.fmt, r, op.cols)
+            elif op.kind == "moe":
+                uniq, remap = np.unique(op.ids, return_inverse=True)
+                U = len(uniq)
+                r = min(op.rows, max(8, (1 << 22) // (op.cols * U)))
+                bank = oracle.quantize_q8_0(synthetic.weights(g, U * r, op.cols))
+                ids = remap.reshape(op.ids.shape).astype(np.int32)
+                x = synthetic.activations(g, n_vec * (op.n_active if op.x_per_slot else 1), op.cols)
+                self.calls.append(lambda b=bank, i=ids, x=x, o=op, U=U, r=r:
+                                  oracle.moe_matvec_q8_0(b, i, x, o.x_per_slot, U, o.n_active, r, o.cols, n_vec))
+                self.pass_bytes += U * weight_bytes("q8_0", r, op.cols)
+            else:
+                W = synthetic.weights(g, op.rows, op.cols)
+                xf = synthetic.activations(g, n_vec, op.cols)
+                Wq, xq, mult, shift = oracle.int8_workload(W, xf)
+                self.calls.append(lambda W=Wq, x=xq, m=mult, s=shift: oracle.matvec_i8_requant(W, x, m, s))
+                self.pass_bytes += op.rows * op.cols + 8 * op.rows
+        self.n_shapes = len(distinct)
 
     def run_pass(self):
-        for (_, r, cols, blocks, x) in self.slabs:
-            self.oracle.matvec(self.fmt, blocks, x, r, cols)
+        for c in self.calls:
+            c()
         return self.pass_bytes
 
     def describe(self, passes):
-        return (f"{passes} passes; each = the first rows (~4M weights) of each of the {len(self.slabs)} "
-                f"distinct {self.model} matrix shapes, {self.pass_bytes / 1e6:.1f} MB of {self.fmt}, "
-                f"n_vec={self.n_vec}, single-threaded C oracle with f64 accumulation")
+        what = {"dense": "the first rows (~4M weights) of each of the {n} distinct {m} matrix shapes",
+                "moe": "the first layer's routing for each of the {n} MoE launch shapes, over a bank of only "
+                       "its distinct experts cut to ~4M weights",
+                "int8": "each of the {n} int8 matrices whole, oracle requant recipe"}[self.kind]
+        return (f"{passes} passes; each = " + what.format(n=self.n_shapes, m=self.model) +
+                f", {self.pass_bytes / 1e6:.1f} MB of {self.fmt} weights, n_vec={self.n_vec}, "
+                f"single-threaded C oracle (f64 accumulation for the float formats)")
 
     def timed(self, budget_s):
         done, n, t0 = 0, 0, time.perf_counter()
@@ -343,6 +501,22 @@ class OracleSample:
 
 
 # ----------------------------------------------------------------- main
+
+def describe_workload(args, model, fmt, ops, kind):
+    if args.shape:
+        return f"{len(ops)} distinct {args.shape} {fmt} matrices per step, n_vec={args.n_vec}"
+    if kind == "dense":
+        fused = WORKLOADS[args.workload][3]
+        note = " with q|k|v and gate|up row-fused (same input)" if fused else ", every projection its own call"
+        return (f"{model} decode token, {fmt}, n_vec={args.n_vec}: {len(ops)} matvecs "
+                f"(all projections + lm_head){note}")
+    if kind == "moe":
+        return (f"MoE decode, {MOE_LAYERS} layers x (gate|up 1536x2048 + down 2048x768) per expert, "
+                f"128 experts, 8 active per token drawn uniformly per layer, {fmt}, n_vec={args.n_vec}: "
+                f"{len(ops)} expert-indexed launches")
+    return (f"int8 GEMV + per-row requant, {INT8_COPIES} distinct copies of each of 1024x3072 and 3072x1024, "
+            f"n_vec={args.n_vec}: {len(ops)} launches")
+
 
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
@@ -362,15 +536,12 @@ def main():
     args = ap.parse_args()
 
     world, rank, local_rank = dist_env()
-    model, fmt, shapes = workload_matrices(args.workload, args.shape, args.format)
-    fused_note = (" with q|k|v and gate|up row-fused (same input)" if WORKLOADS[args.workload][2]
-                  else ", every projection its own call")
-    config = {"workload": (f"{model} decode token, {fmt}, n_vec={args.n_vec}: "
-                           f"{len(shapes)} matvecs (all projections + lm_head){fused_note}") if not args.shape else
-                          (f"{len(shapes)} distinct {args.shape} {fmt} matrices per step, n_vec={args.n_vec}"),
-              "model_shape": model, "format": fmt, "n_vec": args.n_vec, "matvecs_per_step": len(shapes),
-              "l2": "inputs larger than L2 (all weights distinct, 7.97 GB Q8_0 / 4.2 GB Q4_0 per step)"
-              if model == "8b-dense" else "all weights distinct per step",
+    model, fmt, ops = workload_ops(args.workload, args.n_vec, args.shape, args.format)
+    kind = WORKLOADS[args.workload][0] if not args.shape else "dense"
+    config = {"workload": describe_workload(args, model, fmt, ops, kind),
+              "model_shape": model, "format": fmt, "n_vec": args.n_vec, "launches_per_step": len(ops),
+              "l2": (f"inputs larger than L2: every launch reads its own weights, "
+                     f"{sum(op.weight_bytes() for op in ops) / 1e9:.2f} GB per step"),
               "seed": synthetic.SEED_BASE + 2}
 
     if args.impl == "reference":
@@ -407,7 +578,7 @@ def main():
 
     step = Step(args.workload, args.n_vec, device, synthetic.SEED_BASE + 2 + rank, args.shape, args.format)
     graph = step.capture()
-    events = LaunchEvents(len(shapes), _cudart())
+    events = LaunchEvents(len(ops), _cudart())
     graph_ev = step.capture(events)
 
     def barrier():
@@ -428,29 +599,38 @@ def main():
         end.synchronize()
         dev_ms = start.elapsed_time(end) / args.steps
         # ---- per-launch durations (event pairs around each launch), same steps
-        per_launch = np.zeros(len(shapes))
+        per_launch = np.zeros(len(ops))
         for _ in range(args.steps):
             graph_ev.replay()
             per_launch += np.array(events.durations_ms())
         per_launch /= args.steps
         # ---- end to end: pinned host x in, y out, every step
         x_host = step.x_all.cpu().pin_memory()
-        y_host = torch.empty(step.y_all.shape, dtype=torch.float32).pin_memory()
-        for _ in range(2):
+        ids_host = step.ids_all.cpu().pin_memory()
+        y_host = torch.empty(step.y_all.shape, dtype=step.y_all.dtype).pin_memory()
+
+        def e2e_step():
             step.x_all.copy_(x_host, non_blocking=True)
+            if step.ids_bytes:
+                step.ids_all.copy_(ids_host, non_blocking=True)
             graph.replay()
             y_host.copy_(step.y_all, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
         barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record()
         for _ in range(args.steps):
-            step.x_all.copy_(x_host, non_blocking=True)
-            graph.replay()
-            y_host.copy_(step.y_all, non_blocking=True)
+            e2e_step()
         e1.record()
         e1.synchronize()
         e2e_ms = e0.elapsed_time(e1) / args.steps
     clk = clocks.summary()
+    # a wait that timed out inside a kernel leaves its mark here: such a run is not a measurement
+    import quantized_weight_matvec_hq_gb300 as hq
+    fault = hq.hq_device_fault()
+    if fault:
+        raise SystemExit(f"device fault word {fault:#x} during the timed run")
 
     if world > 1:
         dev_ms, e2e_ms = max_over_ranks([dev_ms, e2e_ms], device)
@@ -466,13 +646,13 @@ def main():
     # the mean launch duration is the step's device time over the launch count.
     # The event pairs of the per-shape breakdown add a few microseconds per
     # launch and break the programmatic-launch overlap: a breakdown only.
-    alg = np.array([weight_bytes(fmt, r, c) + 4 * args.n_vec * (r + c) for (_, r, c) in shapes], dtype=np.float64)
+    alg = np.array(step.alg_bytes, dtype=np.float64)
     achieved = float(alg.sum() / (dev_ms / 1e3) / 1e9)
     traffic = read_traffic(args.traffic_file, args.workload, args.n_vec, args.shape)
     kernel_ms = float(per_launch.sum())
     by_shape = {}
-    for (nm, r, c), ms, b in zip(shapes, per_launch, alg):
-        k = f"{nm} {r}x{c}"
+    for op, ms, b in zip(ops, per_launch, alg):
+        k = f"{op.name.rstrip('0123456789_')} {op.rows}x{op.cols}"
         d = by_shape.setdefault(k, [0.0, 0.0, 0])
         d[0] += ms
         d[1] += b
@@ -485,23 +665,23 @@ def main():
         "metric": "quant-matvec weight GB/s", "value": round(value, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dev_ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp32 accumulate over " + fmt, "data": "synthetic", "config": config,
+        "dtype": ("int32 accumulate, int8 requant" if fmt == "i8" else "fp32 accumulate over " + fmt), "data": "synthetic", "config": config,
         "tok_per_s": round(1e3 / dev_ms * world, 2),
         "frac_of_hbm": round(value / world / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": (round(traffic / len(shapes)) if traffic is not None else None),
+                     "traffic": (round(traffic / len(ops)) if traffic is not None else None),
                      "traffic_unit": "DRAM bytes read+written per launch (mean over the step), from ncu",
-                     "algorithmic_bytes_per_launch": round(float(alg.sum()) / len(shapes)),
+                     "algorithmic_bytes_per_launch": round(float(alg.sum()) / len(ops)),
                      "peak_source": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs), burst",
                      "kernel": "matvec_tma_kernel (every launch of the step)",
-                     "launches_per_step": len(shapes),
-                     "mean_launch_us": round(dev_ms * 1e3 / len(shapes), 3)},
+                     "launches_per_step": len(ops),
+                     "mean_launch_us": round(dev_ms * 1e3 / len(ops), 3)},
         "per_shape_event_pairs": shapes_out,
         "per_shape_event_pairs_ms_per_step": round(kernel_ms, 4),
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
-                "h2d_bytes_per_step": int(step.x_bytes), "d2h_bytes_per_step": int(step.y_bytes)},
-        "gpu_launches": len(shapes) * args.steps,
+                "h2d_bytes_per_step": int(step.x_bytes + step.ids_bytes), "d2h_bytes_per_step": int(step.y_bytes)},
+        "gpu_launches": len(ops) * args.steps,
         "clocks": clk,
     }
     if not args.no_cpu_baseline and not args.shape:

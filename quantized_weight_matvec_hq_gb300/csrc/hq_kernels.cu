@@ -79,6 +79,9 @@ struct PolQ8_0 {
     static constexpr int kXElemBytes = 4;           // fp32 activations
     static constexpr int kUnits = 8;                // blocks per chunk, split across consumer warps
     static constexpr bool kSwizzle = false;
+    static constexpr int kConsWarps = 2;            // memory-bound: few warps per CTA, more CTAs
+    static constexpr int kConsWarpsFewAcc = 2;
+    static constexpr bool kComputeBound = false;
     using Acc = float2;
     using Red = float;
 
@@ -158,6 +161,29 @@ struct PolQ8_0 {
     __device__ __forceinline__ static Red finish(const Acc &a) { return a.x + a.y; }
 };
 
+// Q4_0 nibble decode with one and-or per element: a nibble at bit position
+// p in {0, 4, 8, 12} of a word, masked in place and ORed into the exponent of
+// 2^23, is the fp32 value 2^23 + q * 2^p (exact: the mantissa has 23 bits);
+// adding -(2^23 + 8 * 2^p) leaves (q - 8) * 2^p exactly.  A pair of adjacent
+// quant bytes always lies in one 16-bit half of a word (the upper half is
+// shifted down first), so a pair of low nibbles is at bits (0, 8) and a pair
+// of high nibbles at bits (4, 12) -- one bias pair each -- and the 2^p
+// factors are undone once per block.
+// The exponent bits live in a register the compiler cannot see through, so
+// that mask-and-OR stays one lop3 with the mask as its immediate (with both
+// constants immediate it would take two instructions).
+__device__ __forceinline__ uint32_t opaque_magic() {
+    uint32_t m;
+    asm volatile("mov.b32 %0, 0x4B000000;" : "=r"(m));
+    return m;
+}
+template <uint32_t MASK>
+__device__ __forceinline__ float nib(uint32_t w, uint32_t magic) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "n"(MASK), "r"(magic));   // (w & MASK) | magic
+    return __uint_as_float(r);
+}
+
 struct PolQ4_0 {
     static constexpr int kBlockBytes = 18;
     static constexpr int kChunkCols = 256;          // 8 blocks
@@ -166,7 +192,10 @@ struct PolQ4_0 {
     static constexpr int kXElemBytes = 4;
     static constexpr int kUnits = 8;
     static constexpr bool kSwizzle = false;
-    using Acc = float2;
+    static constexpr int kConsWarps = 4;            // nibble decode is ALU-heavy: more warps hide its latency
+    static constexpr int kConsWarpsFewAcc = 3;      // n_vec 1 (two rows per lane): three CTAs fit an SM
+    static constexpr bool kComputeBound = true;     // decode, not HBM, sets the pace
+    using Acc = float2;                             // (elements at nibble bits 0/4, at bits 8/12) x 2^-8
     using Red = float;
 
     template <int NV, int R, int B0, int NB>
@@ -174,8 +203,10 @@ struct PolQ4_0 {
                                                    const uint8_t *__restrict__ xt8, int lane,
                                                    Acc (&acc)[R][NV]) {
         const float *xt = reinterpret_cast<const float *>(xt8);
-        constexpr int NCH = (R * NV >= 4) ? 1 : 2;
-        const float2 kOff = make_float2(-8388616.0f, -8388616.0f);  // -(2^23 + 8)
+        const float2 kBiasLo = make_float2(-8388616.0f, -8390656.0f);   // -(2^23 + 8), -(2^23 + 8 * 2^8)
+        const float2 kBiasHi = make_float2(-8388736.0f, -8421376.0f);   // -(2^23 + 8 * 2^4), -(2^23 + 8 * 2^12)
+        const float2 kSixteenth = make_float2(0.0625f, 0.0625f);
+        const uint32_t magic = opaque_magic();
         const uint4 *rowp[R];
         uint4 c0[R];
 #pragma unroll
@@ -185,50 +216,51 @@ struct PolQ4_0 {
         }
 #pragma unroll
         for (int b = B0; b < B0 + NB; ++b) {
-            // window = 16-byte units b, b+1; block b starts at its byte 2b
-            uint32_t lo[R][8], hi[R][8], sw[R];
+            // window = 16-byte units b, b+1: block b's scale is window bytes 2b, 2b+1
+            // and its quant byte t is window byte 2b + 2 + t (low nibble: element t,
+            // high nibble: element t + 16)
+            uint32_t win[R][8], sw[R];
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const uint4 c1 = rowp[r][b + 1];
-                const uint32_t win[8] = {c0[r].x, c0[r].y, c0[r].z, c0[r].w, c1.x, c1.y, c1.z, c1.w};
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    lo[r][k] = win[k] & 0x0F0F0F0Fu;
-                    hi[r][k] = (win[k] >> 4) & 0x0F0F0F0Fu;
-                }
-                sw[r] = win[b >> 1];
+                win[r][0] = c0[r].x; win[r][1] = c0[r].y; win[r][2] = c0[r].z; win[r][3] = c0[r].w;
+                win[r][4] = c1.x; win[r][5] = c1.y; win[r][6] = c1.z; win[r][7] = c1.w;
+                sw[r] = win[r][b >> 1];
                 c0[r] = c1;
             }
-            float2 s[R][NV][NCH];
+            // per row and vector: sums of the low-nibble elements (x: bits 0, y: bits 8)
+            // and of the high-nibble elements (x: bits 4, y: bits 12)
+            float2 slo[R][NV], shi[R][NV];
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int v = 0; v < NV; ++v)
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) s[r][v][c] = make_float2(0.f, 0.f);
+                for (int v = 0; v < NV; ++v) slo[r][v] = shi[r][v] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
                 float4 xv[NV];
 #pragma unroll
                 for (int v = 0; v < NV; ++v)
                     xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * b + 4 * g);
+                const bool high = g >= 4;                   // elements 16..31: high nibbles
 #pragma unroll
                 for (int r = 0; r < R; ++r) {
-                    float f[4];
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int e = 4 * g + i;                  // element of the block
-                        const int o = 2 * b + 2 + (e & 15);       // window byte holding it
-                        const uint32_t src = (e < 16) ? lo[r][o >> 2] : hi[r][o >> 2];
-                        f[i] = byte_as_float(src, o & 3);
-                    }
-                    const float2 q01 = fadd2(make_float2(f[0], f[1]), kOff);
-                    const float2 q23 = fadd2(make_float2(f[2], f[3]), kOff);
+                    for (int h = 0; h < 2; ++h) {
+                        const int t = (4 * g + 2 * h) & 15;     // first quant byte of the pair
+                        const int o = 2 * b + 2 + t;            // its window byte (even)
+                        const uint32_t w = (o & 2) ? (win[r][o >> 2] >> 16) : win[r][o >> 2];
+                        float2 q;
+                        if (!high) {
+                            q = fadd2(make_float2(nib<0xFu>(w, magic), nib<0xF00u>(w, magic)), kBiasLo);
+                        } else {
+                            q = fadd2(make_float2(nib<0xF0u>(w, magic), nib<0xF000u>(w, magic)), kBiasHi);
+                        }
 #pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        float2 &sv = s[r][v][g % NCH];
-                        sv = ffma2(q01, make_float2(xv[v].x, xv[v].y), sv);
-                        sv = ffma2(q23, make_float2(xv[v].z, xv[v].w), sv);
+                        for (int v = 0; v < NV; ++v) {
+                            const float2 xp = h ? make_float2(xv[v].z, xv[v].w) : make_float2(xv[v].x, xv[v].y);
+                            float2 &sv = high ? shi[r][v] : slo[r][v];
+                            sv = ffma2(q, xp, sv);
+                        }
                     }
                 }
             }
@@ -236,13 +268,10 @@ struct PolQ4_0 {
             for (int r = 0; r < R; ++r) {
                 const unsigned short hb = (b & 1) ? (unsigned short)(sw[r] >> 16) : (unsigned short)(sw[r] & 0xffffu);
                 const float d = __half2float(__ushort_as_half(hb));
-                const float2 dd = make_float2(d, d);
+                const float2 dd = make_float2(d, d * 0.00390625f);          // bits 8/12 carry 2^8 more
 #pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    float2 t = s[r][v][0];
-                    if (NCH == 2) t = fadd2(t, s[r][v][NCH - 1]);
-                    acc[r][v] = ffma2(dd, t, acc[r][v]);
-                }
+                for (int v = 0; v < NV; ++v)
+                    acc[r][v] = ffma2(dd, ffma2(shi[r][v], kSixteenth, slo[r][v]), acc[r][v]);
             }
         }
     }
@@ -256,6 +285,9 @@ struct PolI8 {
     static constexpr int kXElemBytes = 1;
     static constexpr int kUnits = 8;                // 16-byte units per chunk
     static constexpr bool kSwizzle = true;
+    static constexpr int kConsWarps = 2;
+    static constexpr int kConsWarpsFewAcc = 2;
+    static constexpr bool kComputeBound = false;
     using Acc = int;
     using Red = int;
 
@@ -308,7 +340,6 @@ __device__ __forceinline__ int requant_i8(int acc, int mult, int shift) {
 
 // ------------------------------------------------------------------ kernel arguments / layout
 
-constexpr int kConsWarps = 2;       // consumer warps per CTA; warp w takes the fills n = w mod 2
 constexpr int kMaxSplit = 8;        // CTAs per cluster when K is split
 
 struct KArgs {
@@ -332,6 +363,10 @@ struct KArgs {
     int x_per_slot;
 };
 
+// Consumer warps per CTA for a format and accumulator count.
+template <class P, int NV, int R>
+__host__ __device__ constexpr int cons_warps() { return (NV * R <= 2) ? P::kConsWarpsFewAcc : P::kConsWarps; }
+
 template <class P, int NV, int R, bool MOE>
 struct Layout {
     static constexpr int TR = 32 * R;                                   // rows per tile
@@ -342,7 +377,7 @@ struct Layout {
     static_assert(WT % kAlign == 0 && ST % kAlign == 0, "stage alignment");
     static constexpr size_t kMiscBytes = 16 + (MOE ? 4 * kMaxPairs * 4 : 0);   // abort flag, MoE tables
     __host__ __device__ static size_t red_off(int s) { return (size_t)s * ST; }
-    __host__ __device__ static size_t part_off(int s) { return red_off(s) + (size_t)kConsWarps * TR * NV * 4; }
+    __host__ __device__ static size_t part_off(int s) { return red_off(s) + (size_t)cons_warps<P, NV, R>() * TR * NV * 4; }
     __host__ __device__ static size_t bar_off(int s) { return part_off(s) + (size_t)kMaxSplit * TR * NV * 4; }
     __host__ __device__ static size_t misc_off(int s) { return bar_off(s) + (size_t)(2 * s + 2) * 8; }
     __host__ __device__ static size_t total(int s) { return misc_off(s) + kMiscBytes + kAlign; }
@@ -391,14 +426,14 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int c0,
 
 // ------------------------------------------------------------------ the kernel
 //
-// CTA = 4 consumer warps + 1 producer warp, several CTAs per SM (each with its
-// own producer: one thread issuing copies cannot keep HBM busy for a whole
-// SM).  The producer walks the CTA's work items (row tiles, or (expert group,
+// CTA = CW consumer warps (the format's kConsWarps) + 1 producer warp, several
+// CTAs per SM (each with its own producer: one thread issuing copies cannot
+// keep HBM busy for a whole SM).  The producer walks the CTA's work items (row tiles, or (expert group,
 // row tile) for MoE) and fills one stage of the CTA's ring per K chunk.
 // Fill n (chunk j of a tile, counted over the CTA's items) lands in stage
 // n mod S and is consumed whole by warp n mod CW, which owns the tile's 32*R
-// rows (one per lane); S is a multiple of CW, so every stage has one owner.  A tile ends with a fixed-order reduction over the four
-// warps; with a K split, the CTAs of a cluster then combine their partials
+// rows (one per lane); S is a multiple of CW, so every stage has one owner.
+// A tile ends with a fixed-order reduction over the CW warps; with a K split, the CTAs of a cluster then combine their partials
 // through DSMEM.
 //
 // Programmatic dependent launch: the kernel lets the next one in the stream
@@ -406,13 +441,18 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int c0,
 // (weights are never written by another kernel), and waits for the previous
 // kernel only before it touches x or y.
 
-// CTAs per SM the kernel is compiled for: 4 when a lane holds few accumulators
-// (96 registers), 2 when it holds many.
-template <int NV, int R>
-constexpr int ctas_per_sm() { return (NV * R <= 2) ? 5 : 3; }
+// CTAs per SM the kernel is compiled for (its register cap follows): more
+// when a lane holds few accumulators, fewer when it holds many or the CTA has
+// four consumer warps.
+template <class P, int NV, int R>
+constexpr int ctas_per_sm() {
+    return cons_warps<P, NV, R>() >= 8 ? 2
+         : cons_warps<P, NV, R>() >= 4 ? ((NV * R <= 2) ? 3 : 2)
+                                        : ((NV * R <= 2) ? 5 : 3);
+}
 
 template <class P, int NV, int R, bool MOE>
-__global__ void __launch_bounds__(32 * (kConsWarps + 1), ctas_per_sm<NV, R>())
+__global__ void __launch_bounds__(32 * (cons_warps<P, NV, R>() + 1), ctas_per_sm<P, NV, R>())
 matvec_tma_kernel(const __grid_constant__ KArgs a) {
     using L = Layout<P, NV, R, MOE>;
     using Acc = typename P::Acc;
@@ -437,7 +477,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nthreads = blockDim.x;
-    constexpr int CW = kConsWarps;                  // S % CW == 0 (see make_plan)
+    constexpr int CW = cons_warps<P, NV, R>();      // S % CW == 0 (see make_plan)
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -767,6 +807,16 @@ hq_status encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, ui
     return HQ_OK;
 }
 
+// Largest K split (CTAs per cluster); HQ_MAX_KSPLIT overrides it for tuning.
+int max_ksplit() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("HQ_MAX_KSPLIT");
+        v = e ? std::max(1, std::min(kMaxSplit, atoi(e))) : kMaxSplit;
+    }
+    return v;
+}
+
 // Deeper rings when fewer CTAs share an SM (HQ_ADAPTIVE_RING=0 turns it off, for comparison).
 bool adaptive_ring() {
     static int v = -1;
@@ -788,7 +838,7 @@ bool prefer_double_buffer() {
     return v == 1;
 }
 
-// Launch geometry: ctas_per_sm<NV,R>() CTAs per SM, the stage ring sized to
+// Launch geometry: ctas_per_sm<P,NV,R>() CTAs per SM, the stage ring sized to
 // share the SM's shared memory among them.  Row tiles are 32*R rows; when
 // there are too few to fill every CTA slot, K is split across a cluster of up
 // to 8 CTAs, never beyond one wave.
@@ -797,20 +847,25 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     using L = Layout<P, NV, R, MOE>;
     Plan p;
     const size_t budget = (size_t)dev.max_smem_optin;
-    const int want = ctas_per_sm<NV, R>();
+    const int want = ctas_per_sm<P, NV, R>();
+    constexpr int CW = cons_warps<P, NV, R>();
     // two stages per consumer warp (a double buffer each), more when room allows
-    p.stages = 2 * kConsWarps;
-    while (L::total(p.stages + kConsWarps) * want <= budget && p.stages < 4 * kConsWarps) p.stages += kConsWarps;
+    p.stages = 2 * CW;
+    while (L::total(p.stages + CW) * want <= budget && p.stages < 4 * CW) p.stages += CW;
     p.smem = L::total(p.stages);
     const int regs = std::max(32, regs_per_thread);
-    const long long by_regs = 65536 / (32 * (kConsWarps + 1) * ((regs + 7) / 8 * 8));
+    const long long by_regs = 65536 / (32 * (CW + 1) * ((regs + 7) / 8 * 8));
     const long long per_sm = std::max<long long>(1, std::min<long long>({by_regs, (long long)want,
                                                                           (long long)(budget / p.smem)}));
     const long long slots = (long long)dev.num_sms * per_sm;
     int ks = 1;
-    while (ks < 8 && n_work * ks * 2 <= slots && n_chunks >= 2 * ks) ks *= 2;
+    while (ks < max_ksplit() && n_work * ks * 2 <= slots && n_chunks >= 2 * ks) ks *= 2;
     p.ksplit = ks;
-    if (ks == 1) {
+    if (ks == 1 && P::kComputeBound) {
+        // every slot filled, tiles strided over the CTAs: each SM then holds
+        // about the same number of tiles, which is what a decode-bound kernel needs
+        p.grid = (int)std::min<long long>(n_work, slots);
+    } else if (ks == 1) {
         // the same number of tiles for every CTA: with HBM shared fairly, CTAs then finish together
         const long long per_cta = (n_work + slots - 1) / slots;
         p.grid = (int)((n_work + per_cta - 1) / per_cta);
@@ -822,7 +877,7 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     if (adaptive_ring()) {
         const long long resident = std::max<long long>(1, (p.grid + dev.num_sms - 1) / dev.num_sms);
         int st = p.stages;
-        while (st + kConsWarps <= 16 && L::total(st + kConsWarps) * resident <= budget) st += kConsWarps;
+        while (st + CW <= 16 && L::total(st + CW) * resident <= budget) st += CW;
         p.stages = st;
         p.smem = L::total(st);
     }
@@ -869,7 +924,7 @@ hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
     if (p.grid <= 0) return HQ_OK;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
-    cfg.blockDim = dim3((unsigned)(32 * (kConsWarps + 1)), 1, 1);
+    cfg.blockDim = dim3((unsigned)(32 * (cons_warps<P, NV, R>() + 1)), 1, 1);
     cfg.dynamicSmemBytes = p.smem;
     cfg.stream = stream;
     cudaLaunchAttribute attr[2];
@@ -891,13 +946,17 @@ hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
     return HQ_OK;
 }
 
+// Rows per lane: two when a lane holds few vectors' accumulators; for Q4_0
+// always two, since the second row shares the x loads and adds independent
+// work to a warp whose decode, not HBM, is the limit.
 template <class P>
-constexpr int rows_per_lane(int nv) { return nv >= 3 ? 2 : 1; }
+constexpr int rows_per_lane(int nv) {
+    return (nv >= 3 || std::is_same<P, PolQ4_0>::value) ? 2 : 1;
+}
 
-template <class P, int NV>
-hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y, const int32_t *mult,
-                   const int32_t *shift, long long rows, long long cols, cudaStream_t stream) {
-    constexpr int R = rows_per_lane<P>(NV);
+template <class P, int NV, int R>
+hq_status dense_nv_r(const DeviceInfo &dev, const void *W, const void *x, void *y, const int32_t *mult,
+                     const int32_t *shift, long long rows, long long cols, cudaStream_t stream) {
     constexpr bool kI8 = std::is_same<P, PolI8>::value;
     KArgs a = {};
     long long row_bytes;
@@ -929,6 +988,13 @@ hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y,
     a.n_vec = NV;
     const Plan p = make_plan<P, NV, R, false>(dev, a.num_tiles, a.n_chunks, kernel_regs<P, NV, R, false>());
     return launch_tma<P, NV, R, false>(a, p, stream);
+}
+
+template <class P, int NV>
+hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y, const int32_t *mult,
+                   const int32_t *shift, long long rows, long long cols, cudaStream_t stream) {
+    constexpr int R = rows_per_lane<P>(NV);
+    return dense_nv_r<P, NV, R>(dev, W, x, y, mult, shift, rows, cols, stream);
 }
 
 template <class P>
