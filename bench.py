@@ -666,7 +666,7 @@ def main():
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dev_ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": ("int32 accumulate, int8 requant" if fmt == "i8" else "fp32 accumulate over " + fmt), "data": "synthetic", "config": config,
-        "tok_per_s": round(1e3 / dev_ms * world, 2),
+        "tok_per_s": round(1e3 / dev_ms * world * args.n_vec, 2),     # n_vec tokens (verify width) per step
         "frac_of_hbm": round(value / world / peak, 4),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),

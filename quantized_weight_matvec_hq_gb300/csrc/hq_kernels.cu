@@ -376,11 +376,14 @@ struct Layout {
     static constexpr int ST = WT + XT;                                  // stage bytes
     static_assert(WT % kAlign == 0 && ST % kAlign == 0, "stage alignment");
     static constexpr size_t kMiscBytes = 16 + (MOE ? 4 * kMaxPairs * 4 : 0);   // abort flag, MoE tables
+    // s = ring stages, ks = CTAs per cluster along K (the gather buffer exists only when ks > 1)
     __host__ __device__ static size_t red_off(int s) { return (size_t)s * ST; }
     __host__ __device__ static size_t part_off(int s) { return red_off(s) + (size_t)cons_warps<P, NV, R>() * TR * NV * 4; }
-    __host__ __device__ static size_t bar_off(int s) { return part_off(s) + (size_t)kMaxSplit * TR * NV * 4; }
-    __host__ __device__ static size_t misc_off(int s) { return bar_off(s) + (size_t)(2 * s + 2) * 8; }
-    __host__ __device__ static size_t total(int s) { return misc_off(s) + kMiscBytes + kAlign; }
+    __host__ __device__ static size_t bar_off(int s, int ks) {
+        return part_off(s) + (ks > 1 ? (size_t)ks * TR * NV * 4 : 0);
+    }
+    __host__ __device__ static size_t misc_off(int s, int ks) { return bar_off(s, ks) + (size_t)(2 * s + 2) * 8; }
+    __host__ __device__ static size_t total(int s, int ks) { return misc_off(s, ks) + kMiscBytes + kAlign; }
 };
 
 // MoE groups: (token, slot) pairs sorted by expert, cut into groups of at most
@@ -467,10 +470,10 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
     const int S = a.stages;
     Red *red = reinterpret_cast<Red *>(smem + L::red_off(S));
     Red *part = reinterpret_cast<Red *>(smem + L::part_off(S));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off(S));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off(S, a.ksplit));
     uint64_t *empty = full + S;
     uint64_t *gather_bar = empty + S;           // K split: the leader CTA counts the others' partials
-    int *misc = reinterpret_cast<int *>(smem + L::misc_off(S));
+    int *misc = reinterpret_cast<int *>(smem + L::misc_off(S, a.ksplit));
     volatile int *abort_flag = misc;
     const MoeTables mt{misc + 4, misc + 4 + kMaxPairs, misc + 4 + 2 * kMaxPairs,
                        misc + 4 + 3 * kMaxPairs, misc + 1};
@@ -851,8 +854,8 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     constexpr int CW = cons_warps<P, NV, R>();
     // two stages per consumer warp (a double buffer each), more when room allows
     p.stages = 2 * CW;
-    while (L::total(p.stages + CW) * want <= budget && p.stages < 4 * CW) p.stages += CW;
-    p.smem = L::total(p.stages);
+    while (L::total(p.stages + CW, 1) * want <= budget && p.stages < 4 * CW) p.stages += CW;
+    p.smem = L::total(p.stages, 1);
     const int regs = std::max(32, regs_per_thread);
     const long long by_regs = 65536 / (32 * (CW + 1) * ((regs + 7) / 8 * 8));
     const long long per_sm = std::max<long long>(1, std::min<long long>({by_regs, (long long)want,
@@ -874,13 +877,13 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     }
     // the ring takes the shared memory the SM's resident CTAs leave: fewer CTAs
     // per SM get deeper rings, so an SM keeps about the same bytes in flight
-    if (adaptive_ring()) {
-        const long long resident = std::max<long long>(1, (p.grid + dev.num_sms - 1) / dev.num_sms);
-        int st = p.stages;
-        while (st + CW <= 16 && L::total(st + CW) * resident <= budget) st += CW;
-        p.stages = st;
-        p.smem = L::total(st);
-    }
+    const long long resident = std::max<long long>(1, (p.grid + dev.num_sms - 1) / dev.num_sms);
+    int st = p.stages;
+    while (st > CW && L::total(st, ks) * resident > budget) st -= CW;     // room for the gather buffer
+    if (adaptive_ring())
+        while (st + CW <= 16 && L::total(st + CW, ks) * resident <= budget) st += CW;
+    p.stages = st;
+    p.smem = L::total(st, ks);
     return p;
 }
 
@@ -946,12 +949,13 @@ hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
     return HQ_OK;
 }
 
-// Rows per lane: two when a lane holds few vectors' accumulators; for Q4_0
-// always two, since the second row shares the x loads and adds independent
-// work to a warp whose decode, not HBM, is the limit.
+// Rows per lane: two for Q4_0 at one or two vectors (the second row shares the
+// x loads and adds independent work to a warp whose decode, not HBM, is the
+// limit); one otherwise -- with three or more vectors a 64-row stage plus its
+// x tile leaves room for too few CTAs per SM.
 template <class P>
 constexpr int rows_per_lane(int nv) {
-    return (nv >= 3 || std::is_same<P, PolQ4_0>::value) ? 2 : 1;
+    return (std::is_same<P, PolQ4_0>::value && nv <= 2) ? 2 : 1;
 }
 
 template <class P, int NV, int R>
