@@ -138,6 +138,55 @@ def load_peaks():
     return 6800.0, "fallback"
 
 
+def read_probe_gbs(device, gib=2, reps=5):
+    """A read-only HBM reference: a torch sum over a 2 GiB fp32 buffer (far
+    above L2), timed with CUDA events.  Not part of the product path."""
+    import torch
+    buf = torch.ones(gib << 28, dtype=torch.float32, device=device)
+    buf.sum()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        buf.sum()
+    e1.record()
+    e1.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    n = buf.numel() * 4
+    del buf
+    return n / (ms / 1e3) / 1e9
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), for the oracle baseline line."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name:"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def fp32_flops(ops, n_vec):
+    """FP32 multiply-add flops of a step: 2 per weight per vector (MoE: per chosen
+    (token, slot) pair); None for the int8 path, which is not fp32 arithmetic."""
+    total = 0
+    for op in ops:
+        if op.kind == "int8":
+            return None
+        pairs = n_vec * op.n_active if op.kind == "moe" else n_vec
+        total += 2 * op.rows * op.cols * pairs
+    return total
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -562,7 +611,8 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
                 "config": config,
                 "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                 "sample": samp.describe(args.steps) + " (one pass per step)"},
+                                 "sample": samp.describe(args.steps) + " (one pass per step)",
+                                 "cpu": cpu_model()},
                 "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                         "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
@@ -640,6 +690,7 @@ def main():
         return
 
     peak, peak_kind = load_peaks()
+    probe = read_probe_gbs(device)
     value = aggregate_value(world, step.weight_bytes, dev_ms)
     e2e = aggregate_value(world, step.weight_bytes, e2e_ms)
     # Roofline of the matvec kernel: the step consists of its launches only, so
@@ -677,6 +728,10 @@ def main():
                      "kernel": "matvec_tma_kernel (every launch of the step)",
                      "launches_per_step": len(ops),
                      "mean_launch_us": round(dev_ms * 1e3 / len(ops), 3)},
+        "hbm_references": {"measured_copy_gbs": peak, "read_probe_gbs": round(probe, 1),
+                           "spec_gbs": 8000.0, "frac_of_read_probe": round(achieved / probe, 4),
+                           "frac_of_spec": round(achieved / 8000.0, 4),
+                           "read_probe": "torch sum over a 2 GiB fp32 buffer, CUDA events, after the timed region"},
         "per_shape_event_pairs": shapes_out,
         "per_shape_event_pairs_ms_per_step": round(kernel_ms, 4),
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
@@ -684,10 +739,31 @@ def main():
         "gpu_launches": len(ops) * args.steps,
         "clocks": clk,
     }
+    # FP32 roof: where the step's flops per byte exceed the ridge of the FP32
+    # pipe (SMs x 128 FMA lanes x 2 flops x the sampled SM clock) over the HBM
+    # copy bandwidth, the FP32 pipe, not HBM, is the lower roof
+    flops = fp32_flops(ops, args.n_vec)
+    if flops is not None and clk.get("sm_mhz"):
+        n_sms = torch.cuda.get_device_properties(device).multi_processor_count
+        fp32_peak = n_sms * 128 * 2 * clk["sm_mhz"] * 1e6 / 1e12
+        tflops = flops / (dev_ms / 1e3) / 1e12
+        line["fp32_roof"] = {"achieved_tflops": round(tflops, 2), "peak_tflops": round(fp32_peak, 1),
+                             "frac": round(tflops / fp32_peak, 4),
+                             "flops_per_byte": round(flops / float(alg.sum()), 2),
+                             "ridge_flops_per_byte": round(fp32_peak * 1e3 / peak, 2),
+                             "peak_basis": f"{n_sms} SMs x 128 FP32 FMA/clk x 2 x {clk['sm_mhz']} MHz"}
+        if flops / float(alg.sum()) > fp32_peak * 1e3 / peak:
+            line["roofline"].update({"bound": "alu", "achieved": round(tflops, 2), "peak": round(fp32_peak, 1),
+                                     "unit": "TFLOP/s", "frac": round(tflops / fp32_peak, 4),
+                                     "peak_source": line["fp32_roof"]["peak_basis"] +
+                                     " (derived from unit counts and the sampled clock)"})
+    if fmt == "q4_0" and args.n_vec <= 2:
+        line["roofline"]["limiter"] = ("nibble decode issue rate (one lop3 on the ALU pipe, one fadd2 + ffma2 "
+                                       "pair on the FMA pipe per two weights), not HBM")
     if not args.no_cpu_baseline and not args.shape:
         gbs, desc, el = OracleSample(args.workload, args.n_vec).timed(args.cpu_budget)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": desc, "seconds": round(el, 2)}
+                                "sample": desc, "seconds": round(el, 2), "cpu": cpu_model()}
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()

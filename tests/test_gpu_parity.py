@@ -177,10 +177,13 @@ def _sampled_rows(rows, n=24, width=5):
 
 
 @pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
-@pytest.mark.parametrize("rows,cols", [(14336, 4096), (4096, 14336), (1024, 4096)])
+@pytest.mark.parametrize("rows,cols", [(28672, 4096), (6144, 4096), (4096, 4096), (14336, 4096),
+                                       (4096, 14336), (1024, 4096)])
 def test_full_size_8b_shapes_sampled(hq, fmt, rows, cols):
-    """The 8B-dense decode shapes at full size, in the bench's launch
-    configuration; the oracle computes sampled rows one range at a time."""
+    """The 8B-dense decode shapes at full size -- the fused gate|up and q|k|v
+    and o, down of the bench's decode token, and the unfused gate, k -- in the
+    bench's launch configuration; the oracle computes sampled rows one range
+    at a time."""
     g = synthetic.rng(synthetic.SEED_BASE + 2)
     W = synthetic.weights(g, rows, cols)
     blocks = quant(fmt, W)
@@ -194,23 +197,38 @@ def test_full_size_8b_shapes_sampled(hq, fmt, rows, cols):
             assert_within(y[:, lo:hi], y_ref, T, f"{fmt} {rows}x{cols} n_vec={n_vec} rows {lo}:{hi}")
 
 
-def test_full_size_lm_heads_sampled(hq):
+@pytest.mark.parametrize("fmt,rows,cols", [("q8_0", 151936, 1024), ("q8_0", 128256, 4096),
+                                           ("q4_0", 128256, 4096)])
+def test_full_size_lm_heads_sampled(hq, fmt, rows, cols):
     """The tied Qwen3-0.6B lm_head (151936 x 1024) and the 8B lm_head
-    (128256 x 4096, 558 MB of Q8_0), n_vec = 1, sampled rows."""
-    for rows, cols in ((151936, 1024), (128256, 4096)):
-        g = synthetic.rng(synthetic.SEED_BASE + 7)
-        blocks = np.empty((rows, cols // 32 * 34), np.uint8)
-        step = 8192
-        for r0 in range(0, rows, step):                    # quantize in slabs to bound host memory
-            r1 = min(rows, r0 + step)
-            blocks[r0:r1] = oracle.quantize_q8_0(synthetic.weights(g, r1 - r0, cols))
-        x = synthetic.activations(g, 1, cols)
+    (128256 x 4096: 558 MB of Q8_0, 296 MB of Q4_0), n_vec = 1, sampled rows."""
+    g = synthetic.rng(synthetic.SEED_BASE + 7)
+    blocks = np.empty((rows, cols // 32 * (34 if fmt == "q8_0" else 18)), np.uint8)
+    step = 8192
+    for r0 in range(0, rows, step):                        # quantize in slabs to bound host memory
+        r1 = min(rows, r0 + step)
+        blocks[r0:r1] = quant(fmt, synthetic.weights(g, r1 - r0, cols))
+    x = synthetic.activations(g, 1, cols)
+    y = gpu_matvec(hq, fmt, blocks, x, rows, cols)
+    f = hq.hq_device_fault()
+    assert f == 0, f"{rows}x{cols}: fault word {f:#x} ({hq.hq_last_error()})"
+    for lo, hi in _sampled_rows(rows, n=40):
+        y_ref, T = oracle.matvec_rows(fmt, blocks, x, rows, cols, lo, hi)
+        assert_within(y[:, lo:hi], y_ref, T, f"{fmt} lm_head {rows}x{cols} rows {lo}:{hi}")
+
+
+@pytest.mark.parametrize("rows,cols", sorted({(r, c) for (_, r, c) in
+                                              synthetic.QWEN3_0_6B_LAYER + synthetic.fuse_same_input(synthetic.QWEN3_0_6B_LAYER)}))
+def test_qwen3_0_6b_layer_shapes_full(hq, rows, cols):
+    """Every Qwen3-0.6B-shaped decode matvec (unfused and with q|k|v, gate|up
+    row-fused), Q8_0, every output checked, n_vec 1 and 2."""
+    g = synthetic.rng(synthetic.SEED_BASE + 1)
+    blocks = quant("q8_0", synthetic.weights(g, rows, cols))
+    for n_vec in (1, 2):
+        x = synthetic.activations(g, n_vec, cols)
+        y_ref, T = oracle.matvec("q8_0", blocks, x, rows, cols)
         y = gpu_matvec(hq, "q8_0", blocks, x, rows, cols)
-        f = hq.hq_device_fault()
-        assert f == 0, f"{rows}x{cols}: fault word {f:#x} ({hq.hq_last_error()})"
-        for lo, hi in _sampled_rows(rows, n=40):
-            y_ref, T = oracle.matvec_rows("q8_0", blocks, x, rows, cols, lo, hi)
-            assert_within(y[:, lo:hi], y_ref, T, f"lm_head {rows}x{cols} rows {lo}:{hi}")
+        assert_within(y, y_ref, T, f"qwen3 {rows}x{cols} n_vec={n_vec}")
 
 
 # ---------------------------------------------------------------- int8 requant
@@ -284,9 +302,12 @@ def gpu_moe(hq, bank, ids, x, x_per_slot, n_experts, n_active, rows, cols, n_vec
     return y.cpu().numpy()
 
 
-@pytest.mark.parametrize("x_per_slot,rows,cols", [(False, 768, 2048), (True, 2048, 768)])
+@pytest.mark.parametrize("x_per_slot,rows,cols", [(False, 768, 2048), (True, 2048, 768), (False, 1536, 2048)])
 @pytest.mark.parametrize("n_vec", [1, 4, 8])
 def test_moe_128_experts_top8(hq, x_per_slot, rows, cols, n_vec):
+    """128 experts, top-8: gate (768x2048, x shared by the slots), down
+    (2048x768, x per slot) and the row-fused gate|up (1536x2048) the bench
+    launches."""
     n_experts, n_active = 128, 8
     bank, ids, x = _moe_case(n_experts, n_active, rows, cols, n_vec, 3000 + n_vec, x_per_slot)
     y = gpu_moe(hq, bank, ids, x, x_per_slot, n_experts, n_active, rows, cols, n_vec)
