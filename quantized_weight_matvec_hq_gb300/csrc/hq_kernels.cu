@@ -375,7 +375,7 @@ struct Layout {
     static constexpr int XT = ((NV * P::kChunkCols * P::kXElemBytes + kAlign - 1) / kAlign) * kAlign;
     static constexpr int ST = WT + XT;                                  // stage bytes
     static_assert(WT % kAlign == 0 && ST % kAlign == 0, "stage alignment");
-    static constexpr size_t kMiscBytes = 16 + (MOE ? 4 * kMaxPairs * 4 : 0);   // abort flag, MoE tables
+    static constexpr size_t kMiscBytes = 16 + (MOE ? 5 * kMaxPairs * 4 : 0);   // abort flag, MoE tables
     // s = ring stages, ks = CTAs per cluster along K (the gather buffer exists only when ks > 1)
     __host__ __device__ static size_t red_off(int s) { return (size_t)s * ST; }
     __host__ __device__ static size_t part_off(int s) { return red_off(s) + (size_t)cons_warps<P, NV, R>() * TR * NV * 4; }
@@ -389,7 +389,7 @@ struct Layout {
 // MoE groups: (token, slot) pairs sorted by expert, cut into groups of at most
 // NV pairs sharing one expert; group g covers sorted[gstart[g] .. + gsize[g]).
 struct MoeTables {
-    int *sorted, *gstart, *gsize, *gexpert, *n_groups;
+    int *sorted, *gstart, *gsize, *gexpert, *n_groups, *ids;    // ids: the call's expert ids, staged
 };
 
 template <class P, bool MOE>
@@ -476,7 +476,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
     int *misc = reinterpret_cast<int *>(smem + L::misc_off(S, a.ksplit));
     volatile int *abort_flag = misc;
     const MoeTables mt{misc + 4, misc + 4 + kMaxPairs, misc + 4 + 2 * kMaxPairs,
-                       misc + 4 + 3 * kMaxPairs, misc + 1};
+                       misc + 4 + 3 * kMaxPairs, misc + 1, misc + 4 + 4 * kMaxPairs};
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nthreads = blockDim.x;
@@ -495,14 +495,18 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
     if constexpr (MOE) {
         // ids may come from the previous kernel (a router): wait for it first
         griddep_wait();
-        // Group the (token, slot) pairs by expert; every CTA derives the same table.
+        // Group the (token, slot) pairs by expert; every CTA derives the same
+        // table.  The ids are read from global memory once, in parallel, and
+        // every later look-up is a shared-memory read.
         const int P_ = a.n_vec * a.n_active;
+        for (int p = threadIdx.x; p < P_; p += nthreads) mt.ids[p] = a.ids[p];
+        __syncthreads();
         for (int p = threadIdx.x; p < P_; p += nthreads) {
-            const int e = a.ids[p];
+            const int e = mt.ids[p];
             const long long ke = (e >= 0 && e < a.n_experts) ? e : a.n_experts;
             int rank = 0;
             for (int q = 0; q < P_; ++q) {
-                const int eq = a.ids[q];
+                const int eq = mt.ids[q];
                 const long long kq = (eq >= 0 && eq < a.n_experts) ? eq : a.n_experts;
                 rank += (kq < ke) || (kq == ke && q < p);
             }
@@ -512,10 +516,10 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
         if (threadIdx.x == 0) {
             int ng = 0, bad = 0;
             for (int i = 0; i < P_;) {
-                const int e = a.ids[mt.sorted[i]];
+                const int e = mt.ids[mt.sorted[i]];
                 if (e < 0 || e >= a.n_experts) { bad = 1; ++i; continue; }
                 int j = i + 1;
-                while (j < P_ && j - i < NV && a.ids[mt.sorted[j]] == e) ++j;
+                while (j < P_ && j - i < NV && mt.ids[mt.sorted[j]] == e) ++j;
                 mt.gstart[ng] = i; mt.gsize[ng] = j - i; mt.gexpert[ng] = e; ++ng;
                 i = j;
             }
@@ -525,7 +529,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
         __syncthreads();
         if (blockIdx.x == 0) {                     // outputs of invalid ids become NaN
             for (int p = 0; p < P_; ++p) {
-                const int e = a.ids[p];
+                const int e = mt.ids[p];
                 if (e >= 0 && e < a.n_experts) continue;
                 for (long long r = threadIdx.x; r < a.rows; r += nthreads)
                     reinterpret_cast<float *>(a.y)[(long long)p * a.rows + r] = __int_as_float(0x7fc00000);
@@ -820,6 +824,16 @@ int max_ksplit() {
     return v;
 }
 
+// A ring no deeper than the CTA's own fills (HQ_RING_CAP=0 turns it off, for comparison).
+bool ring_cap() {
+    static int v = -1;
+    if (v < 0) {
+        const char *e = getenv("HQ_RING_CAP");
+        v = (e && atoi(e) == 0) ? 0 : 1;
+    }
+    return v == 1;
+}
+
 // Deeper rings when fewer CTAs share an SM (HQ_ADAPTIVE_RING=0 turns it off, for comparison).
 bool adaptive_ring() {
     static int v = -1;
@@ -882,6 +896,15 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     while (st > CW && L::total(st, ks) * resident > budget) st -= CW;     // room for the gather buffer
     if (adaptive_ring())
         while (st + CW <= 16 && L::total(st + CW, ks) * resident <= budget) st += CW;
+    if (ring_cap()) {
+        // a CTA never has more stages than fills: the shared memory it leaves
+        // lets the next kernel's CTAs become resident (and start their weight
+        // copies) while this one drains
+        const long long items = (ks > 1) ? 1 : (n_work + p.grid - 1) / std::max(p.grid, 1);
+        const long long fills = items * ((n_chunks + ks - 1) / ks);
+        const long long need = std::max<long long>(CW, (fills + CW - 1) / CW * CW);
+        if (need < st) st = (int)need;
+    }
     p.stages = st;
     p.smem = L::total(st, ks);
     return p;
