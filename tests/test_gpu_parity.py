@@ -159,6 +159,24 @@ def test_closed_forms_on_gpu(hq, fmt):
     assert np.all(y[:, 10] == 0)
 
 
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("scale", [1e-30, 1e-6, 1e6, 1e15])
+def test_x_magnitudes(hq, fmt, scale):
+    """x far from N(0, 1): the one- and two-vector decodes rescale x by 2^64,
+    read quants as fp32 subnormals and apply the quant offset per block; the
+    wider decode reads x as stored.  All stay within the tolerance (tiny x
+    falls back on its absolute term)."""
+    rows, cols = 300, 2048
+    g = synthetic.rng(90)
+    blocks = quant(fmt, synthetic.weights(g, rows, cols))
+    for n_vec in (1, 2, 4):
+        x = (synthetic.activations(g, n_vec, cols) * np.float32(scale)).astype(np.float32)
+        y_ref, T = oracle.matvec(fmt, blocks, x, rows, cols)
+        y = gpu_matvec(hq, fmt, blocks, x, rows, cols)
+        assert np.all(np.isfinite(y))
+        assert_within(y, y_ref, T, f"{fmt} x*{scale:g} n_vec={n_vec}")
+
+
 def test_deterministic_and_stream(hq):
     rows, cols = 4096, 4096
     g = synthetic.rng(79)
