@@ -69,8 +69,9 @@ class Op:
     """One launch of a step: a dense matvec, an expert-indexed MoE matvec or an
     int8 requant GEMV, with the bytes it reads and writes."""
 
-    def __init__(self, kind, name, rows, cols, fmt, n_experts=0, n_active=0, x_per_slot=0, ids=None):
+    def __init__(self, kind, name, rows, cols, fmt, n_experts=0, n_active=0, x_per_slot=0, ids=None, label=None):
         self.kind, self.name, self.rows, self.cols, self.fmt = kind, name, rows, cols, fmt
+        self.label = label or name                   # the matrix's role, without layer or copy index
         self.n_experts, self.n_active, self.x_per_slot, self.ids = n_experts, n_active, x_per_slot, ids
 
     def x_elems(self, n_vec):
@@ -113,13 +114,13 @@ def workload_ops(name, n_vec, shape=None, fmt=None, seed=synthetic.SEED_BASE + 2
         E, A, H, F = synthetic.MOE_N_EXPERTS, synthetic.MOE_N_ACTIVE, synthetic.MOE_HIDDEN, synthetic.MOE_FFN
         for layer in range(MOE_LAYERS):
             ids = synthetic.expert_ids(g, n_vec, A, E)
-            ops.append(Op("moe", f"gate_up{layer}", 2 * F, H, fmt, E, A, 0, ids))
-            ops.append(Op("moe", f"down{layer}", H, F, fmt, E, A, 1, ids))
+            ops.append(Op("moe", f"gate_up{layer}", 2 * F, H, fmt, E, A, 0, ids, label="gate_up"))
+            ops.append(Op("moe", f"down{layer}", H, F, fmt, E, A, 1, ids, label="down"))
         return model, fmt, ops
     ops = []
     for i in range(INT8_COPIES):
         for (r, c) in synthetic.INT8_SHAPES:
-            ops.append(Op("int8", f"i8_{r}x{c}_{i}", r, c, fmt))
+            ops.append(Op("int8", f"i8_{r}x{c}_{i}", r, c, fmt, label="i8"))
     return model, fmt, ops
 
 
@@ -703,7 +704,7 @@ def main():
     kernel_ms = float(per_launch.sum())
     by_shape = {}
     for op, ms, b in zip(ops, per_launch, alg):
-        k = f"{op.name.rstrip('0123456789_')} {op.rows}x{op.cols}"
+        k = f"{op.label} {op.rows}x{op.cols}"
         d = by_shape.setdefault(k, [0.0, 0.0, 0])
         d[0] += ms
         d[1] += b
