@@ -205,6 +205,18 @@ hq_status hq_requant_i32_debug(const int32_t *acc, const int32_t *mult, const in
 #define HQ_FAULT_EXPERT_ID    2u   /* an expert id outside [0, n_experts)      */
 hq_status hq_device_fault(uint32_t *fault);
 
+/*
+ * hq_selftest_wait_timeout -- test-only exercise of the failure path: one CTA
+ * of one warp waits on an mbarrier that nothing arrives on, with the matvec
+ * kernels' bounded wait but a limit of `cycles` SM clock cycles
+ * (1 <= cycles <= 4e9).  The wait gives up, sets HQ_FAULT_WAIT_TIMEOUT in the
+ * fault word with CTA 0 and the consumer bit recorded, and the kernel returns:
+ * nothing faults, traps or hangs, and the context stays usable.  Read the
+ * result with hq_device_fault().
+ * Source: none on the pages (a property of this implementation's waits).
+ */
+hq_status hq_selftest_wait_timeout(int64_t cycles, hq_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

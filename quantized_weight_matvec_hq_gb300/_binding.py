@@ -54,6 +54,7 @@ _SIGS = {
     "hq_requant_params": ([_vp, _i64, _vp, _vp], _int),
     "hq_requant_i32_debug": ([_vp, _vp, _vp, _vp, _i64, _i64, _vp], _int),
     "hq_device_fault": ([_vp], _int),
+    "hq_selftest_wait_timeout": ([_i64, _vp], _int),
 }
 
 
@@ -159,6 +160,11 @@ def hq_requant_params(M, n: int, mult, shift) -> int:
 def hq_requant_i32_debug(acc, mult, shift, y, n: int, rows: int, stream=None) -> int:
     return _check(lib().hq_requant_i32_debug(_addr(acc), _addr(mult), _addr(shift), _addr(y), n, rows,
                                              _stream(stream)))
+
+
+def hq_selftest_wait_timeout(cycles: int, stream=None) -> int:
+    """Test-only: a bounded wait that nothing completes; sets the fault word."""
+    return _check(lib().hq_selftest_wait_timeout(int(cycles), _stream(stream)))
 
 
 def hq_device_fault() -> int:

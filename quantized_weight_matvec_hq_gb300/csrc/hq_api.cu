@@ -198,6 +198,14 @@ hq_status hq_requant_i32_debug(const int32_t *acc, const int32_t *mult, const in
     return finish(launch_requant_debug(acc, mult, shift, y, n, rows, (cudaStream_t)stream));
 }
 
+hq_status hq_selftest_wait_timeout(int64_t cycles, hq_stream_t stream) {
+    if (cycles < 1 || cycles > 4000000000LL) return set_error(HQ_ERR_SHAPE, "cycles %lld not in [1, 4e9]", (long long)cycles);
+    DeviceInfo *dev = nullptr;
+    hq_status st = device_info(&dev);
+    if (st != HQ_OK) return st;
+    return finish(launch_wait_timeout_selftest(dev->fault, cycles, (cudaStream_t)stream));
+}
+
 hq_status hq_device_fault(uint32_t *fault) {
     if (!fault) return set_error(HQ_ERR_NULL, "fault must be non-null");
     DeviceInfo *dev = nullptr;

@@ -66,13 +66,14 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return ok != 0;
 }
 
-// Bounded wait on phase `parity` of an mbarrier.  `abort` is CTA-shared: once
+// Bounded wait on phase `parity` of an mbarrier (at most limit_cycles SM cycles).  `abort` is CTA-shared: once
 // any wait in the CTA (or, through the fault word, in any CTA) has timed out,
 // later waits return false at once so the kernel drains in bounded time.  The clock and
 // the global fault word are only looked at every 256 polls, so a waiting warp
 // notices a completed phase within one poll.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          volatile int *abort, uint32_t *fault) {
+                                          volatile int *abort, uint32_t *fault,
+                                          long long limit_cycles = kWaitTimeoutCycles) {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = sm_cycles();
 #pragma unroll 1
@@ -82,7 +83,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
             if (*abort) return false;
             // only another wait's timeout aborts; a data fault (bad expert id) does not
             if (*(volatile uint32_t *)fault & kFaultWaitTimeout) { *abort = 1; return false; }
-            if (sm_cycles() - t0 > kWaitTimeoutCycles) {
+            if (sm_cycles() - t0 > limit_cycles) {
                 // bits 8..31 keep where the first timeout happened: the CTA and
                 // whether the waiter was a consumer (bit 8 set) or the producer
                 const uint32_t site = ((blockIdx.x & 0x7fffffu) << 9) | ((threadIdx.x < 128u) ? 0x100u : 0u);

@@ -33,6 +33,7 @@ hq_status launch_moe_q8_0(const void *W_bank, const int32_t *ids, const float *x
 hq_status launch_matvec_i8(const int8_t *W, const int8_t *x, const int32_t *mult,
                            const int32_t *shift, int8_t *y, int64_t rows, int64_t cols, int n_vec,
                            cudaStream_t stream);
+hq_status launch_wait_timeout_selftest(uint32_t *fault, int64_t cycles, cudaStream_t stream);
 hq_status launch_requant_debug(const int32_t *acc, const int32_t *mult, const int32_t *shift,
                                int8_t *y, int64_t n, int64_t rows, cudaStream_t stream);
 hq_status launch_quantize(int fmt, const float *W, void *out, float *scale, int64_t rows,

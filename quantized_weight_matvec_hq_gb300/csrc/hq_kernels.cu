@@ -1011,6 +1011,21 @@ __global__ void requant_debug_kernel(const int32_t *__restrict__ acc, const int3
         y[i] = (int8_t)requant_i8(acc[i], mult[i % rows], shift[i % rows]);
 }
 
+// Test-only: a bounded wait on an mbarrier nothing arrives on (see
+// hq_selftest_wait_timeout in the header).
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(uint32_t *fault, long long limit_cycles) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0) mbar_wait(smem_u32(&bar), 0, &abort_flag, fault, limit_cycles);
+    __syncwarp();
+}
+
 #endif  // HQ_PART == 2
 
 // ------------------------------------------------------------------ host side
@@ -1332,6 +1347,13 @@ hq_status launch_matvec_i8(const int8_t *W, const int8_t *x, const int32_t *mult
     matvec_i8_plain_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(W, x, mult, shift, y, rows, cols, n_vec);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "int8 matvec launch: %s", cudaGetErrorString(e));
+    return HQ_OK;
+}
+
+hq_status launch_wait_timeout_selftest(uint32_t *fault, int64_t cycles, cudaStream_t stream) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(fault, (long long)cycles);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "self-test launch: %s", cudaGetErrorString(e));
     return HQ_OK;
 }
 

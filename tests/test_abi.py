@@ -70,6 +70,9 @@ def test_host_validation_before_any_launch(hq):
     # quantizers
     assert L.hq_quantize_q8_0(fake, fake, 4, 40, 0) == hq.HQ_ERR_SHAPE
     assert L.hq_quantize_q4_0(0, fake, 4, 64, 0) == hq.HQ_ERR_NULL
+    # the wait-timeout self-test bounds its limit before touching a device
+    assert L.hq_selftest_wait_timeout(0, 0) == hq.HQ_ERR_SHAPE
+    assert L.hq_selftest_wait_timeout(5_000_000_000, 0) == hq.HQ_ERR_SHAPE
     with pytest.raises(hq.HQError):
         hq.hq_matvec_q8_0(0, 0, 0, 4, 64, 1, stream=0)
 
