@@ -157,7 +157,9 @@ hq_status hq_moe_matvec_q8_0(const void *W_bank, const int32_t *expert_ids,
  * hq_quantize_i8_rows: scale[o] = max|W[o,:]|/127 (fp32),
  *   Wq = round(W/scale) clamped to [-127,127]; with rows = 1 this is the
  *   static per-tensor activation quantizer.
- * Requires rows >= 1 and cols % 32 == 0 (i8: cols >= 1); W 4-byte aligned.
+ * Requires rows >= 1 and cols % 32 == 0 (i8: cols >= 1).  Alignment: Q8_0 and
+ * Q4_0 take W 16-byte aligned and out 2-byte aligned; the int8 quantizer takes
+ * W and scale 4-byte aligned.  HQ_ERR_ALIGN otherwise.
  * Source: "One Native Stack ...", section "The Unified Quant Core" (formats
  * taken verbatim from ggml); "Blue -- porting zen-nano ...", section
  * "Quantization recipe (validated)".

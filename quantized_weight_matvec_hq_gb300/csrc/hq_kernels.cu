@@ -642,31 +642,27 @@ __device__ __forceinline__ void consume_chunk(const uint8_t *wt, const uint8_t *
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *m, int c0, int c1) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];"
-                 ::"l"(reinterpret_cast<uint64_t>(m)), "r"(c0), "r"(c1) : "memory");
-}
-
 // ------------------------------------------------------------------ the kernel
 //
-// CTA = CW consumer warps (the format's kConsWarps) + 1 producer warp, several
+// CTA = CW consumer warps (cons_warps<P,NV,R>) + 1 producer warp, several
 // CTAs per SM (each with its own producer: one thread issuing copies cannot
-// keep HBM busy for a whole SM).  The producer walks the CTA's work items (row tiles, or (expert group,
-// row tile) for MoE) and fills one stage of the CTA's ring per K chunk.
-// Fill n (chunk j of a tile, counted over the CTA's items) lands in stage
-// n mod S and is consumed whole by warp n mod CW, which owns the tile's 32*R
-// rows (one per lane); S is a multiple of CW, so every stage has one owner.
-// A tile ends with a fixed-order reduction over the CW warps; with a K split, the CTAs of a cluster then combine their partials
+// keep HBM busy for a whole SM).  The producer walks the CTA's work items
+// (row tiles, or (expert group, row tile) for MoE) and fills one stage of the
+// CTA's ring per K chunk.  Fill n (chunk j of a tile, counted over the CTA's
+// items) lands in stage n mod S and is consumed whole by warp n mod CW, which
+// owns the tile's 32*R rows (R per lane); S is a multiple of CW, so every
+// stage has one owner.  A tile ends with a fixed-order reduction over the CW
+// warps; with a K split, the CTAs of a cluster then combine their partials
 // through DSMEM.
 //
 // Programmatic dependent launch: the kernel lets the next one in the stream
-// start as soon as it is resident, prefetches its first weight tiles into L2
-// (weights are never written by another kernel), and waits for the previous
-// kernel only before it touches x or y.
+// start as soon as it is resident, issues the weight copies of its first
+// stages at once (weights are never written by another kernel), and waits for
+// the previous kernel only before it touches x, expert ids or y.
 
 // CTAs per SM the kernel is compiled for (its register cap follows): more
 // when a lane holds few accumulators, fewer when it holds many or the CTA has
-// four consumer warps.
+// four or more consumer warps.
 template <class P, int NV, int R>
 constexpr int ctas_per_sm() {
     return cons_warps<P, NV, R>() >= 8 ? 2
@@ -1080,17 +1076,6 @@ bool adaptive_ring() {
     if (v < 0) {
         const char *e = getenv("HQ_ADAPTIVE_RING");
         v = (e && atoi(e) == 0) ? 0 : 1;
-    }
-    return v == 1;
-}
-
-// Ring depth choice, overridable for tuning: HQ_STAGES_PER_WARP=2 gives every
-// consumer warp a double buffer (8 stages, fewer CTAs per SM).
-bool prefer_double_buffer() {
-    static int v = -1;
-    if (v < 0) {
-        const char *e = getenv("HQ_STAGES_PER_WARP");
-        v = (e && atoi(e) == 2) ? 1 : 0;
     }
     return v == 1;
 }
