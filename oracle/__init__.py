@@ -70,6 +70,10 @@ def lib() -> ctypes.CDLL:
         L.hqo_requant_array.restype = None
         L.hqo_requant_params.argtypes = [_p, _i64, _p, _p]
         L.hqo_requant_params.restype = _int
+        L.hqo_bf16_to_float.argtypes = [ctypes.c_uint16]
+        L.hqo_bf16_to_float.restype = ctypes.c_float
+        L.hqo_lora_delta.argtypes = [_p, _p, _p, ctypes.c_double, _i64, _i64, _i64, _i64, _p, _p]
+        L.hqo_lora_delta.restype = None
         L.hqo_version.restype = _int
         _LIB = L
     return _LIB
@@ -244,6 +248,29 @@ def int8_workload(W: np.ndarray, x: np.ndarray, out_quantile: float = 0.99):
     M = s_w.astype(np.float64) * s_x / s_out
     mult, shift = requant_params(M)
     return Wq, xq, mult, shift
+
+
+# ---------------------------------------------------------------- QLoRA adapter term
+
+def bf16_to_float(h: int) -> float:
+    return float(lib().hqo_bf16_to_float(int(h)))
+
+
+def lora_delta(A: np.ndarray, B: np.ndarray, x: np.ndarray, scale: float):
+    """The QLoRA adapter term scale * B (A x) in f64 and its magnitude T.
+    A: bf16 bits uint16 [rank][cols]; B: bf16 bits uint16 [rows][rank];
+    x: fp32 [n_vec][cols].  Returns (delta, T), f64 [n_vec][rows]."""
+    A = np.ascontiguousarray(A, dtype=np.uint16)
+    B = np.ascontiguousarray(B, dtype=np.uint16)
+    rank, cols = A.shape
+    rows = B.shape[0]
+    assert B.shape[1] == rank
+    x = np.ascontiguousarray(x, dtype=np.float32).reshape(-1, cols)
+    n_vec = x.shape[0]
+    delta = np.empty((n_vec, rows), dtype=np.float64)
+    T = np.empty((n_vec, rows), dtype=np.float64)
+    lib().hqo_lora_delta(_ptr(A), _ptr(B), _ptr(x), float(scale), rank, rows, cols, n_vec, _ptr(delta), _ptr(T))
+    return delta, T
 
 
 def version() -> int:

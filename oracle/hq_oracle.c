@@ -389,4 +389,47 @@ int hqo_requant_params(const double *M, int64_t n, int32_t *mult, int32_t *shift
     return 0;
 }
 
+/* ---------------------------------------------------------------- QLoRA adapter term
+ * [NST] section "The Central Efficiency Thesis", Lemma "QLoRA over the unified
+ * core is exact": y_i = sum_j What_ij x_j + (alpha/r) (B_A (A x))_i, with
+ * A in R^{r x d_in} and B_A in R^{d_out x r} stored in bf16.  The oracle
+ * returns the adapter term alone (the base term is the matvec above), in f64:
+ *   u_k       = sum_j A[k][j] * x[v][j]
+ *   delta[v][i] = scale * sum_k B[i][k] * u_k          (scale = alpha / r)
+ * and T[v][i] = |scale| * sum_k |B[i][k]| * sum_j |A[k][j] * x[v][j]|, the
+ * magnitude the float tolerance is taken against. */
+
+/* bf16 is the upper half of an fp32 bit pattern. */
+float hqo_bf16_to_float(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+void hqo_lora_delta(const uint16_t *A, const uint16_t *B, const float *x, double scale,
+                    int64_t rank, int64_t rows, int64_t cols, int64_t n_vec,
+                    double *delta, double *T)
+{
+    for (int64_t v = 0; v < n_vec; ++v) {
+        for (int64_t i = 0; i < rows; ++i) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < rank; ++k) {
+                double u = 0.0, ua = 0.0;
+                for (int64_t j = 0; j < cols; ++j) {
+                    double p = (double)hqo_bf16_to_float(A[k * cols + j]) * (double)x[v * cols + j];
+                    u += p;
+                    ua += fabs(p);
+                }
+                double b = (double)hqo_bf16_to_float(B[i * rank + k]);
+                acc += b * u;
+                mag += fabs(b) * ua;
+            }
+            delta[v * rows + i] = scale * acc;
+            T[v * rows + i] = fabs(scale) * mag;
+        }
+    }
+}
+
 int hqo_version(void) { return 1; }

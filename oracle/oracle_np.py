@@ -51,6 +51,29 @@ def matvec(fmt: str, blocks: np.ndarray, x: np.ndarray, rows: int, cols: int):
     return y, T
 
 
+def bf16_to_f64(h: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns decoded from the IEEE fields (sign, 8-bit exponent with
+    bias 127, 7-bit fraction), not by reinterpreting bits."""
+    h = np.asarray(h, dtype=np.int64)
+    s = np.where((h >> 15) & 1, -1.0, 1.0)
+    e = (h >> 7) & 0xFF
+    m = (h & 0x7F).astype(np.float64)
+    with np.errstate(over="ignore", invalid="ignore"):
+        normal = s * np.ldexp(1.0 + m / 128.0, (e - 127).astype(np.int64))
+        sub = s * np.ldexp(m / 128.0, -126)
+        special = np.where(m == 0, s * np.inf, np.nan)
+    return np.where(e == 0, sub, np.where(e == 255, special, normal))
+
+
+def lora_delta(A: np.ndarray, B: np.ndarray, x: np.ndarray, scale: float):
+    """scale * B (A x) and its magnitude, f64 matrix products of the decoded factors."""
+    Af, Bf = bf16_to_f64(A), bf16_to_f64(B)
+    X = np.asarray(x, dtype=np.float32).reshape(-1, Af.shape[1]).astype(np.float64)
+    delta = scale * (X @ Af.T) @ Bf.T
+    T = abs(scale) * (np.abs(X) @ np.abs(Af).T) @ np.abs(Bf).T
+    return delta, T
+
+
 # ----------------------------------------------------------- independent quantizers
 # A second, vectorised statement of the same readings (fp32 arithmetic), used
 # to cross-check the C quantizers byte for byte.

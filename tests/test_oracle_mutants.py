@@ -39,6 +39,10 @@ MUTANTS = {
     "q8_scale_254": ("float d = amax / 127.0f;\n            uint16_t dh", "float d = amax / 254.0f;\n            uint16_t dh"),
     "q4_scale_positive": ("float d = m / -8.0f;", "float d = m / 8.0f;"),
     "q4_round_down": ("float t = w[j] / d + 8.5f;", "float t = w[j] / d + 8.0f;"),
+    "lora_A_transposed": ("hqo_bf16_to_float(A[k * cols + j])", "hqo_bf16_to_float(A[j * rank + k])"),
+    "lora_B_transposed": ("hqo_bf16_to_float(B[i * rank + k])", "hqo_bf16_to_float(B[k * rows + i])"),
+    "lora_scale_dropped": ("delta[v * rows + i] = scale * acc;", "delta[v * rows + i] = acc;"),
+    "bf16_shift_15": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
 }
 
 
@@ -67,6 +71,9 @@ def _build_mutant(tmp_path, name):
     L.hqo_requant.restype = ctypes.c_int8
     L.hqo_float_to_half_rne.argtypes = [ctypes.c_float]
     L.hqo_float_to_half_rne.restype = ctypes.c_uint16
+    L.hqo_bf16_to_float.argtypes = [ctypes.c_uint16]
+    L.hqo_bf16_to_float.restype = ctypes.c_float
+    L.hqo_lora_delta.argtypes = [vp, vp, vp, ctypes.c_double, i64, i64, i64, i64, vp, vp]
     return L
 
 
@@ -126,6 +133,17 @@ def _pins_fail(L, golden_dir):
     ref = mids.astype(np.float16).view(np.uint16)
     if any(L.hqo_float_to_half_rne(float(v)) != r for v, r in zip(mids, ref)):
         failed.append("half")
+    # QLoRA adapter term: bf16 values and a non-square brute force
+    if L.hqo_bf16_to_float(0x3F80) != 1.0 or L.hqo_bf16_to_float(0xC2F6) != -123.0:
+        failed.append("bf16")
+    from test_oracle_lora import _case
+    rank, rows, cols, n_vec = 3, 7, 40, 2
+    A, B, x = _case(11, rank, rows, cols, n_vec)
+    d = np.empty((n_vec, rows)); T = np.empty((n_vec, rows))
+    L.hqo_lora_delta(ptr(A), ptr(B), ptr(x), 0.75, rank, rows, cols, n_vec, ptr(d), ptr(T))
+    d_ref, _ = oracle_np.lora_delta(A, B, x, 0.75)
+    if not np.allclose(d, d_ref, rtol=1e-12, atol=1e-14):
+        failed.append("lora")
     return failed
 
 
