@@ -57,7 +57,14 @@ WORKLOADS = {
     "qwen3-0.6b-q8_0-unfused": ("dense", "qwen3-0.6b", "q8_0", False),
     "moe-q8_0": ("moe", "moe-128x8-hidden2048", "q8_0", True),
     "int8-requant": ("int8", "int8-1024x3072+3072x1024", "i8", False),
+    "8b-q8_0-lora": ("dense", "8b-dense", "q8_0", True),
+    "8b-q4_0-lora": ("dense", "8b-dense", "q4_0", True),
 }
+# QLoRA workloads: a bf16 adapter of this rank on every projection (not the
+# lm_head), scale alpha / r = 2 (rank-16 adapters on the attention and FFN
+# projections are the pages' example configuration)
+LORA_RANK = {"8b-q8_0-lora": 16, "8b-q4_0-lora": 16}
+LORA_SCALE = 2.0
 # MoE decode: a stack of this many layers, each with its own bank of experts
 # (128 x (gate|up 1536x2048 + down 2048x768) Q8_0 = 642 MB per layer)
 MOE_LAYERS = 48
@@ -69,9 +76,11 @@ class Op:
     """One launch of a step: a dense matvec, an expert-indexed MoE matvec or an
     int8 requant GEMV, with the bytes it reads and writes."""
 
-    def __init__(self, kind, name, rows, cols, fmt, n_experts=0, n_active=0, x_per_slot=0, ids=None, label=None):
+    def __init__(self, kind, name, rows, cols, fmt, n_experts=0, n_active=0, x_per_slot=0, ids=None, label=None,
+                 lora_rank=0):
         self.kind, self.name, self.rows, self.cols, self.fmt = kind, name, rows, cols, fmt
         self.label = label or name                   # the matrix's role, without layer or copy index
+        self.lora_rank = lora_rank                   # QLoRA adapter rank (0: none)
         self.n_experts, self.n_active, self.x_per_slot, self.ids = n_experts, n_active, x_per_slot, ids
 
     def x_elems(self, n_vec):
@@ -87,12 +96,13 @@ class Op:
         one = weight_bytes(self.fmt, self.rows, self.cols)
         if self.kind == "moe":
             return one * len(np.unique(self.ids))
-        return one
+        return one + 2 * self.lora_rank * (self.rows + self.cols)     # + bf16 adapter factors
 
     def alg_bytes(self, n_vec):
         """Algorithmic bytes of a launch: weights read + x read + y written (+ expert ids)."""
         el = 1 if self.kind == "int8" else 4
         extra = self.ids.size * 4 if self.kind == "moe" else 0
+        extra += 2 * 4 * self.lora_rank * n_vec                     # u = A x written, then read
         return self.weight_bytes() + el * (self.x_elems(n_vec) + self.y_elems(n_vec)) + extra
 
 
@@ -107,7 +117,9 @@ def workload_ops(name, n_vec, shape=None, fmt=None, seed=synthetic.SEED_BASE + 2
         return f"single {rows}x{cols}", fmt, [Op("dense", f"m{rows}x{cols}", rows, cols, fmt)] * copies
     kind, model, fmt, fused = WORKLOADS[name]
     if kind == "dense":
-        return model, fmt, [Op("dense", n, r, c, fmt) for (n, r, c) in synthetic.decode_token_shapes(model, fused)]
+        rank = LORA_RANK.get(name, 0)
+        return model, fmt, [Op("dense", n, r, c, fmt, lora_rank=(rank if n != "lm_head" else 0))
+                            for (n, r, c) in synthetic.decode_token_shapes(model, fused)]
     if kind == "moe":
         g = synthetic.rng(seed + 7)
         ops = []
@@ -336,6 +348,7 @@ class Step:
         self.y_all = torch.empty(ny, device=device, dtype=xdt)
         self.ids_all = torch.zeros(max(ni, 4), device=device, dtype=torch.int32)
         self.W, self.x, self.y, self.ids, self.mult, self.shift = [], [], [], [], [], []
+        self.lora = []                              # (A, B, workspace) per op, or None
         for i, op in enumerate(self.ops):
             self.x.append(self.x_all[xo[i]:xo[i] + op.x_elems(n_vec)])
             self.y.append(self.y_all[yo[i]:yo[i] + op.y_elems(n_vec)])
@@ -353,6 +366,13 @@ class Step:
             else:
                 self.mult.append(None)
                 self.shift.append(None)
+            if op.lora_rank:
+                A = torch.randn((op.lora_rank, op.cols), generator=g, device=device).mul_(0.02).to(torch.bfloat16)
+                B = torch.randn((op.rows, op.lora_rank), generator=g, device=device).mul_(0.02).to(torch.bfloat16)
+                ws = torch.empty(op.lora_rank * n_vec, dtype=torch.float32, device=device)
+                self.lora.append((A, B, ws))
+            else:
+                self.lora.append(None)
         torch.cuda.synchronize()
         self.weight_bytes = sum(op.weight_bytes() for op in self.ops)
         self.alg_bytes = [op.alg_bytes(n_vec) for op in self.ops]
@@ -406,7 +426,12 @@ class Step:
         for i, op in enumerate(self.ops):
             if events is not None:
                 events.record_before(i, stream)
-            if op.kind == "dense":
+            if op.kind == "dense" and op.lora_rank:
+                A, B, ws = self.lora[i]
+                fn = hq.hq_matvec_q8_0_lora if op.fmt == "q8_0" else hq.hq_matvec_q4_0_lora
+                fn(self.W[i], self.x[i], A, B, LORA_SCALE, op.lora_rank, ws, self.y[i], op.rows, op.cols, n_vec,
+                   stream=stream)
+            elif op.kind == "dense":
                 fn = hq.hq_matvec_q8_0 if op.fmt == "q8_0" else hq.hq_matvec_q4_0
                 fn(self.W[i], self.x[i], self.y[i], op.rows, op.cols, n_vec, stream=stream)
             elif op.kind == "moe":
@@ -508,6 +533,13 @@ class OracleSample:
                 x = synthetic.activations(g, n_vec, op.cols)
                 self.calls.append(lambda b=blocks, x=x, r=r, c=op.cols: oracle.matvec(self.fmt, b, x, r, c))
                 self.pass_bytes += weight_bytes(self.fmt, r, op.cols)
+                if op.lora_rank:
+                    # the adapter term of the same sampled rows (bf16 bit patterns of N(0, 0.02))
+                    A = (g.standard_normal((op.lora_rank, op.cols)).astype(np.float32) * np.float32(0.02)).view(np.uint32) >> 16
+                    B = (g.standard_normal((r, op.lora_rank)).astype(np.float32) * np.float32(0.02)).view(np.uint32) >> 16
+                    A, B = A.astype(np.uint16), B.astype(np.uint16)
+                    self.calls.append(lambda A=A, B=B, x=x: oracle.lora_delta(A, B, x, LORA_SCALE))
+                    self.pass_bytes += 2 * op.lora_rank * (r + op.cols)
             elif op.kind == "moe":
                 uniq, remap = np.unique(op.ids, return_inverse=True)
                 U = len(uniq)
@@ -558,8 +590,11 @@ def describe_workload(args, model, fmt, ops, kind):
     if kind == "dense":
         fused = WORKLOADS[args.workload][3]
         note = " with q|k|v and gate|up row-fused (same input)" if fused else ", every projection its own call"
+        lora = (f"; a rank-{LORA_RANK[args.workload]} bf16 QLoRA adapter (scale {LORA_SCALE:g}) on every "
+                f"projection, its bytes counted as weights, two kernels per adapted matvec"
+                if args.workload in LORA_RANK else "")
         return (f"{model} decode token, {fmt}, n_vec={args.n_vec}: {len(ops)} matvecs "
-                f"(all projections + lm_head){note}")
+                f"(all projections + lm_head){note}{lora}")
     if kind == "moe":
         return (f"MoE decode, {MOE_LAYERS} layers x (gate|up 1536x2048 + down 2048x768) per expert, "
                 f"128 experts, 8 active per token drawn uniformly per layer, {fmt}, n_vec={args.n_vec}: "
@@ -737,7 +772,7 @@ def main():
         "per_shape_event_pairs_ms_per_step": round(kernel_ms, 4),
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": int(step.x_bytes + step.ids_bytes), "d2h_bytes_per_step": int(step.y_bytes)},
-        "gpu_launches": len(ops) * args.steps,
+        "gpu_launches": sum(2 if op.lora_rank else 1 for op in ops) * args.steps,
         "clocks": clk,
     }
     # FP32 roof: where the step's flops per byte exceed the ridge of the FP32

@@ -103,6 +103,30 @@ hq_status hq_matvec_q4_0(const void *W, const float *x, float *y,
                          int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
 
 /*
+ * hq_matvec_q8_0_lora, hq_matvec_q4_0_lora -- the float matvec of the same
+ * format plus a QLoRA adapter over the frozen quantized base:
+ *   y[v][i] = sum_j w_deq[i][j] x[v][j] + scale * sum_k B[i][k] (sum_j A[k][j] x[v][j]).
+ *   lora_A    : bf16 [rank][cols] (raw bf16 bits), 16-byte aligned.
+ *   lora_B    : bf16 [rows][rank], 2-byte aligned.
+ *   scale     : alpha / r, finite.   rank : 1..64.
+ *   workspace : caller-owned device memory of at least rank * n_vec floats,
+ *               4-byte aligned; it receives u = A x (fp32 [n_vec][rank]) and
+ *               must not be in use by other work until the call's kernels end.
+ * W, x, y, rows, cols, n_vec and the accuracy are as for hq_matvec_q8_0; the
+ * adapter term adds 1e-3 * |scale| * sum_k |B[i][k]| * sum_j |A[k][j] x[v][j]|
+ * to the tolerance.  Two kernels run: the down projection u = A x, then the
+ * matvec, which streams W once and adds scale * B u as it stores y.
+ * Source: "One Native Stack ...", section "The Central Efficiency Thesis",
+ * Lemma "QLoRA over the unified core is exact and base-weight-identical".
+ */
+hq_status hq_matvec_q8_0_lora(const void *W, const float *x, const uint16_t *lora_A,
+                              const uint16_t *lora_B, float scale, int rank, float *workspace,
+                              float *y, int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
+hq_status hq_matvec_q4_0_lora(const void *W, const float *x, const uint16_t *lora_A,
+                              const uint16_t *lora_B, float scale, int rank, float *workspace,
+                              float *y, int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
+
+/*
  * hq_matvec_i8_requant -- per-output-channel int8 GEMV with gemmlowp requant:
  *   acc = sum_j W[o][j] * x[v][j]  (int32; the caller keeps it in range:
  *         |W|, |x| <= 127 and cols < 133,000 always fit),

@@ -412,19 +412,25 @@ void hqo_lora_delta(const uint16_t *A, const uint16_t *B, const float *x, double
                     int64_t rank, int64_t rows, int64_t cols, int64_t n_vec,
                     double *delta, double *T)
 {
+    double u[64], ua[64];                  /* the adapter's rank is at most 64 */
     for (int64_t v = 0; v < n_vec; ++v) {
+        /* the bracket (A x) first, as the Lemma writes it */
+        for (int64_t k = 0; k < rank && k < 64; ++k) {
+            u[k] = 0.0;
+            ua[k] = 0.0;
+            for (int64_t j = 0; j < cols; ++j) {
+                double p = (double)hqo_bf16_to_float(A[k * cols + j]) * (double)x[v * cols + j];
+                u[k] += p;
+                ua[k] += fabs(p);
+            }
+        }
+        /* then B_A applied to it, and the scale */
         for (int64_t i = 0; i < rows; ++i) {
             double acc = 0.0, mag = 0.0;
-            for (int64_t k = 0; k < rank; ++k) {
-                double u = 0.0, ua = 0.0;
-                for (int64_t j = 0; j < cols; ++j) {
-                    double p = (double)hqo_bf16_to_float(A[k * cols + j]) * (double)x[v * cols + j];
-                    u += p;
-                    ua += fabs(p);
-                }
+            for (int64_t k = 0; k < rank && k < 64; ++k) {
                 double b = (double)hqo_bf16_to_float(B[i * rank + k]);
-                acc += b * u;
-                mag += fabs(b) * ua;
+                acc += b * u[k];
+                mag += fabs(b) * ua[k];
             }
             delta[v * rows + i] = scale * acc;
             T[v * rows + i] = fabs(scale) * mag;

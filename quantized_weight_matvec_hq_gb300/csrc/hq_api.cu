@@ -8,6 +8,8 @@
 
 #include <mutex>
 
+#include <cmath>
+
 #include "hq_internal.h"
 
 namespace hq {
@@ -111,14 +113,50 @@ hq_status hq_matvec_q8_0(const void *W, const float *x, float *y, int64_t rows, 
                          int n_vec, hq_stream_t stream) {
     hq_status st = check_float_matvec(W, x, y, rows, cols, n_vec);
     if (st != HQ_OK) return st;
-    return finish(launch_matvec_float_q8_0(W, x, y, rows, cols, n_vec, (cudaStream_t)stream));
+    return finish(launch_matvec_float_q8_0(W, x, y, rows, cols, n_vec, nullptr, (cudaStream_t)stream));
 }
 
 hq_status hq_matvec_q4_0(const void *W, const float *x, float *y, int64_t rows, int64_t cols,
                          int n_vec, hq_stream_t stream) {
     hq_status st = check_float_matvec(W, x, y, rows, cols, n_vec);
     if (st != HQ_OK) return st;
-    return finish(launch_matvec_float_q4_0(W, x, y, rows, cols, n_vec, (cudaStream_t)stream));
+    return finish(launch_matvec_float_q4_0(W, x, y, rows, cols, n_vec, nullptr, (cudaStream_t)stream));
+}
+
+// The float matvec plus the QLoRA adapter term: u = A x into the caller's
+// workspace, then the matvec adds scale * B u as it stores each output.
+static hq_status matvec_lora(int fmt, const void *W, const float *x, const uint16_t *A, const uint16_t *B,
+                             float scale, int rank, float *workspace, float *y, int64_t rows, int64_t cols,
+                             int n_vec, hq_stream_t stream) {
+    hq_status st = check_float_matvec(W, x, y, rows, cols, n_vec);
+    if (st != HQ_OK) return st;
+    if (!A || !B || !workspace) return set_error(HQ_ERR_NULL, "lora_A, lora_B and workspace must be non-null");
+    if (rank < 1 || rank > 64) return set_error(HQ_ERR_SHAPE, "rank %d not in [1,64]", rank);
+    if (!std::isfinite(scale)) return set_error(HQ_ERR_SHAPE, "scale must be finite");
+    if (!aligned(A, 16) || !aligned(B, 2) || !aligned(workspace, 4))
+        return set_error(HQ_ERR_ALIGN, "lora_A must be 16-byte aligned, lora_B 2-byte, workspace 4-byte");
+    cudaStream_t s = (cudaStream_t)stream;
+    st = launch_lora_down(A, x, workspace, rank, cols, n_vec, s);
+    if (st != HQ_OK) return st;
+    LoraArgs l;
+    l.B = B;
+    l.u = workspace;
+    l.scale = scale;
+    l.rank = rank;
+    return finish(fmt == 8 ? launch_matvec_float_q8_0(W, x, y, rows, cols, n_vec, &l, s)
+                           : launch_matvec_float_q4_0(W, x, y, rows, cols, n_vec, &l, s));
+}
+
+hq_status hq_matvec_q8_0_lora(const void *W, const float *x, const uint16_t *lora_A, const uint16_t *lora_B,
+                              float scale, int rank, float *workspace, float *y, int64_t rows, int64_t cols,
+                              int n_vec, hq_stream_t stream) {
+    return matvec_lora(8, W, x, lora_A, lora_B, scale, rank, workspace, y, rows, cols, n_vec, stream);
+}
+
+hq_status hq_matvec_q4_0_lora(const void *W, const float *x, const uint16_t *lora_A, const uint16_t *lora_B,
+                              float scale, int rank, float *workspace, float *y, int64_t rows, int64_t cols,
+                              int n_vec, hq_stream_t stream) {
+    return matvec_lora(4, W, x, lora_A, lora_B, scale, rank, workspace, y, rows, cols, n_vec, stream);
 }
 
 hq_status hq_matvec_i8_requant(const int8_t *W, const int8_t *x, const int32_t *mult,

@@ -22,11 +22,22 @@ hq_status device_info(DeviceInfo **out);            // current device
 hq_status set_error(hq_status st, const char *fmt, ...);
 void *tensor_map_encoder();                         // PFN_cuTensorMapEncodeTiled
 
+// QLoRA adapter epilogue of a float matvec: y += scale * B u, where u = A x
+// was computed by launch_lora_down earlier on the same stream.
+struct LoraArgs {
+    const uint16_t *B = nullptr;    // bf16 [rows][rank]
+    const float *u = nullptr;       // fp32 [n_vec][rank]
+    float scale = 0.f;
+    int rank = 0;                   // 0: no adapter
+};
+
 // Launchers (arguments already validated by the API layer).
 hq_status launch_matvec_float_q8_0(const void *W, const float *x, float *y, int64_t rows,
-                                   int64_t cols, int n_vec, cudaStream_t stream);
+                                   int64_t cols, int n_vec, const LoraArgs *lora, cudaStream_t stream);
 hq_status launch_matvec_float_q4_0(const void *W, const float *x, float *y, int64_t rows,
-                                   int64_t cols, int n_vec, cudaStream_t stream);
+                                   int64_t cols, int n_vec, const LoraArgs *lora, cudaStream_t stream);
+hq_status launch_lora_down(const uint16_t *A, const float *x, float *u, int rank, int64_t cols,
+                           int n_vec, cudaStream_t stream);
 hq_status launch_moe_q8_0(const void *W_bank, const int32_t *ids, const float *x, int x_per_slot,
                           float *y, int64_t n_experts, int n_active, int64_t rows, int64_t cols,
                           int n_vec, cudaStream_t stream);

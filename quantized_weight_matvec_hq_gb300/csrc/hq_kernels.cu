@@ -581,6 +581,10 @@ struct KArgs {
     int n_vec;
     int n_active;
     int x_per_slot;
+    const uint16_t *lora_B;   // QLoRA epilogue (lora_rank > 0): bf16 [rows][lora_rank]
+    const float *lora_u;      //   u = A x, fp32 [n_vec][lora_rank]
+    float lora_scale;         //   y += lora_scale * B u
+    int lora_rank;
 };
 
 // Consumer warps per CTA for a format and accumulator count.
@@ -612,6 +616,17 @@ struct MoeTables {
     int *sorted, *gstart, *gsize, *gexpert, *n_groups, *ids;    // ids: the call's expert ids, staged
 };
 
+// The QLoRA term scale * sum_k B[row][k] * u[v][k] of one output (bf16 B,
+// its bits the upper half of an fp32).
+__device__ __forceinline__ float lora_term(const uint16_t *B, const float *u, float scale, int rank,
+                                           int v, long long row) {
+    const uint16_t *b = B + row * rank;
+    const float *uv = u + (long long)v * rank;
+    float t = 0.f;
+    for (int k = 0; k < rank; ++k) t = fmaf(__uint_as_float((uint32_t)b[k] << 16), uv[k], t);
+    return scale * t;
+}
+
 template <class P, bool MOE>
 __device__ __forceinline__ void store_out(const KArgs &a, const MoeTables &mt, int g, int v,
                                           long long row, typename P::Red val) {
@@ -620,6 +635,7 @@ __device__ __forceinline__ void store_out(const KArgs &a, const MoeTables &mt, i
             (int8_t)requant_i8(val, a.mult[row], a.shift[row]);
     } else {
         const long long p = MOE ? (long long)mt.sorted[mt.gstart[g] + v] : (long long)v;
+        if (!MOE && a.lora_rank > 0) val += lora_term(a.lora_B, a.lora_u, a.lora_scale, a.lora_rank, v, row);
         reinterpret_cast<float *>(a.y)[p * a.rows + row] = val;
     }
 }
@@ -937,7 +953,8 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
 template <int FMT>
 __global__ void __launch_bounds__(256)
 matvec_plain_kernel(const uint8_t *__restrict__ W, const float *__restrict__ x, float *__restrict__ y,
-                    long long rows, long long cols, int n_vec) {
+                    long long rows, long long cols, int n_vec, const uint16_t *lora_B,
+                    const float *lora_u, float lora_scale, int lora_rank) {
     const long long row = (long long)blockIdx.x * 8 + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
@@ -973,7 +990,10 @@ matvec_plain_kernel(const uint8_t *__restrict__ W, const float *__restrict__ x, 
     for (int v = 0; v < n_vec; ++v) {
         float s = acc[v];
         for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-        if (lane == 0) y[(long long)v * rows + row] = s;
+        if (lane == 0) {
+            if (lora_rank > 0) s += lora_term(lora_B, lora_u, lora_scale, lora_rank, v, row);
+            y[(long long)v * rows + row] = s;
+        }
     }
 }
 
@@ -1005,6 +1025,53 @@ __global__ void requant_debug_kernel(const int32_t *__restrict__ acc, const int3
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n;
          i += (long long)gridDim.x * blockDim.x)
         y[i] = (int8_t)requant_i8(acc[i], mult[i % rows], shift[i % rows]);
+}
+
+// QLoRA down projection u[v][k] = sum_j A[k][j] * x[v][j] (A bf16 [rank][cols],
+// cols % 8 == 0): one CTA per adapter row k, eight columns per thread and
+// step, then a fixed-order reduction (warp shuffles, then the warps in order),
+// so u is the same bit for bit on every run.  It lets the matvec that follows
+// start at once (that kernel reads u only after waiting for this one).
+__global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t *__restrict__ A,
+                                                        const float *__restrict__ x, float *__restrict__ u,
+                                                        int rank, long long cols, int n_vec) {
+    griddep_launch_dependents();
+    const int k = blockIdx.x;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float acc[8];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) acc[v] = 0.f;
+    const uint4 *a8 = reinterpret_cast<const uint4 *>(A + (long long)k * cols);
+    for (long long c = threadIdx.x; c < cols / 8; c += blockDim.x) {
+        const uint4 w = a8[c];
+        const float wf[8] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                             __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u),
+                             __uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
+                             __uint_as_float(w.w << 16), __uint_as_float(w.w & 0xffff0000u)};
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            if (v >= n_vec) break;
+            const float4 *xv = reinterpret_cast<const float4 *>(x + (long long)v * cols) + 2 * c;
+            const float4 p = xv[0], q = xv[1];
+            float t = acc[v];
+            t = fmaf(wf[0], p.x, t); t = fmaf(wf[1], p.y, t); t = fmaf(wf[2], p.z, t); t = fmaf(wf[3], p.w, t);
+            t = fmaf(wf[4], q.x, t); t = fmaf(wf[5], q.y, t); t = fmaf(wf[6], q.z, t); t = fmaf(wf[7], q.w, t);
+            acc[v] = t;
+        }
+    }
+    __shared__ float red[8][8];
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        float t = acc[v];
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (lane == 0) red[warp][v] = t;
+    }
+    __syncthreads();
+    if (threadIdx.x < n_vec) {
+        float t = 0.f;
+        for (int w2 = 0; w2 < (int)(blockDim.x >> 5); ++w2) t += red[w2][threadIdx.x];
+        u[(long long)threadIdx.x * rank + k] = t;
+    }
 }
 
 // Test-only: a bounded wait on an mbarrier nothing arrives on (see
@@ -1208,7 +1275,8 @@ constexpr int rows_per_lane(int nv) {
 
 template <class P, int NV, int R>
 hq_status dense_nv_r(const DeviceInfo &dev, const void *W, const void *x, void *y, const int32_t *mult,
-                     const int32_t *shift, long long rows, long long cols, cudaStream_t stream) {
+                     const int32_t *shift, long long rows, long long cols, const LoraArgs *lora,
+                     cudaStream_t stream) {
     constexpr bool kI8 = std::is_same<P, PolI8>::value;
     KArgs a = {};
     long long row_bytes;
@@ -1238,30 +1306,37 @@ hq_status dense_nv_r(const DeviceInfo &dev, const void *W, const void *x, void *
     a.n_chunks = (int)(cols / P::kChunkCols);
     a.num_tiles = (int)((rows + 32 * R - 1) / (32 * R));
     a.n_vec = NV;
+    if (lora && lora->rank > 0) {
+        a.lora_B = lora->B;
+        a.lora_u = lora->u;
+        a.lora_scale = lora->scale;
+        a.lora_rank = lora->rank;
+    }
     const Plan p = make_plan<P, NV, R, false>(dev, a.num_tiles, a.n_chunks, kernel_regs<P, NV, R, false>());
     return launch_tma<P, NV, R, false>(a, p, stream);
 }
 
 template <class P, int NV>
 hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y, const int32_t *mult,
-                   const int32_t *shift, long long rows, long long cols, cudaStream_t stream) {
+                   const int32_t *shift, long long rows, long long cols, const LoraArgs *lora,
+                   cudaStream_t stream) {
     constexpr int R = rows_per_lane<P>(NV);
-    return dense_nv_r<P, NV, R>(dev, W, x, y, mult, shift, rows, cols, stream);
+    return dense_nv_r<P, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
 }
 
 template <class P>
 hq_status dense_dispatch(const DeviceInfo &dev, const void *W, const void *x, void *y,
                          const int32_t *mult, const int32_t *shift, long long rows, long long cols,
-                         int n_vec, cudaStream_t stream) {
+                         int n_vec, const LoraArgs *lora, cudaStream_t stream) {
     switch (n_vec) {
-        case 1: return dense_nv<P, 1>(dev, W, x, y, mult, shift, rows, cols, stream);
-        case 2: return dense_nv<P, 2>(dev, W, x, y, mult, shift, rows, cols, stream);
-        case 3: return dense_nv<P, 3>(dev, W, x, y, mult, shift, rows, cols, stream);
-        case 4: return dense_nv<P, 4>(dev, W, x, y, mult, shift, rows, cols, stream);
-        case 5: return dense_nv<P, 5>(dev, W, x, y, mult, shift, rows, cols, stream);
-        case 6: return dense_nv<P, 6>(dev, W, x, y, mult, shift, rows, cols, stream);
-        case 7: return dense_nv<P, 7>(dev, W, x, y, mult, shift, rows, cols, stream);
-        case 8: return dense_nv<P, 8>(dev, W, x, y, mult, shift, rows, cols, stream);
+        case 1: return dense_nv<P, 1>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
+        case 2: return dense_nv<P, 2>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
+        case 3: return dense_nv<P, 3>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
+        case 4: return dense_nv<P, 4>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
+        case 5: return dense_nv<P, 5>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
+        case 6: return dense_nv<P, 6>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
+        case 7: return dense_nv<P, 7>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
+        case 8: return dense_nv<P, 8>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
         default: return set_error(HQ_ERR_NVEC, "n_vec %d not in [1,8]", n_vec);
     }
 }
@@ -1305,15 +1380,19 @@ hq_status moe_nv(const DeviceInfo &dev, const void *W_bank, const int32_t *ids, 
 // file each) so that the template instantiations build in parallel.
 #if !defined(HQ_PART) || HQ_PART == 0 || HQ_PART == 1
 hq_status HQ_PART_NAME(launch_matvec_float)(const void *W, const float *x, float *y, int64_t rows,
-                                            int64_t cols, int n_vec, cudaStream_t stream) {
+                                            int64_t cols, int n_vec, const LoraArgs *lora,
+                                            cudaStream_t stream) {
     constexpr int FMT = (HQ_PART == 1) ? 1 : 0;
     using P = std::conditional<FMT == 0, PolQ8_0, PolQ4_0>::type;
     DeviceInfo *dev = nullptr;
     hq_status st = device_info(&dev);
     if (st != HQ_OK) return st;
-    if (cols % 256 == 0) return dense_dispatch<P>(*dev, W, x, y, nullptr, nullptr, rows, cols, n_vec, stream);
+    if (cols % 256 == 0) return dense_dispatch<P>(*dev, W, x, y, nullptr, nullptr, rows, cols, n_vec, lora, stream);
     const unsigned grid = (unsigned)((rows + 7) / 8);
-    matvec_plain_kernel<FMT><<<grid, 256, 0, stream>>>((const uint8_t *)W, x, y, rows, cols, n_vec);
+    const LoraArgs none;
+    const LoraArgs &l = lora ? *lora : none;
+    matvec_plain_kernel<FMT><<<grid, 256, 0, stream>>>((const uint8_t *)W, x, y, rows, cols, n_vec,
+                                                       l.B, l.u, l.scale, l.rank);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "matvec launch: %s", cudaGetErrorString(e));
     return HQ_OK;
@@ -1328,10 +1407,18 @@ hq_status launch_matvec_i8(const int8_t *W, const int8_t *x, const int32_t *mult
     hq_status st = device_info(&dev);
     if (st != HQ_OK) return st;
     if (cols % 128 == 0)
-        return dense_dispatch<PolI8>(*dev, W, x, y, mult, shift, rows, cols, n_vec, stream);
+        return dense_dispatch<PolI8>(*dev, W, x, y, mult, shift, rows, cols, n_vec, nullptr, stream);
     matvec_i8_plain_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(W, x, mult, shift, y, rows, cols, n_vec);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "int8 matvec launch: %s", cudaGetErrorString(e));
+    return HQ_OK;
+}
+
+hq_status launch_lora_down(const uint16_t *A, const float *x, float *u, int rank, int64_t cols,
+                           int n_vec, cudaStream_t stream) {
+    lora_down_kernel<<<(unsigned)rank, 256, 0, stream>>>(A, x, u, rank, (long long)cols, n_vec);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "adapter launch: %s", cudaGetErrorString(e));
     return HQ_OK;
 }
 
