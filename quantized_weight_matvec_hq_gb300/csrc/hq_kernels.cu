@@ -1030,20 +1030,43 @@ __global__ void requant_debug_kernel(const int32_t *__restrict__ acc, const int3
 // QLoRA down projection u[v][k] = sum_j A[k][j] * x[v][j] (A bf16 [rank][cols],
 // cols % 8 == 0): one CTA per adapter row k, eight columns per thread and
 // step, then a fixed-order reduction (warp shuffles, then the warps in order),
-// so u is the same bit for bit on every run.  It lets the matvec that follows
-// start at once (that kernel reads u only after waiting for this one).
+// so u is the same bit for bit on every run.  Launched as a programmatic
+// dependent: it becomes resident while the previous kernel drains, loads its
+// row of A, and reads x (which that kernel may write) only after waiting for
+// it; it lets the matvec that follows start at once (that kernel reads u only
+// after waiting for this one).
 __global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t *__restrict__ A,
                                                         const float *__restrict__ x, float *__restrict__ u,
                                                         int rank, long long cols, int n_vec) {
     griddep_launch_dependents();
     const int k = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint4 *a8 = reinterpret_cast<const uint4 *>(A + (long long)k * cols);
+    const long long n8 = cols / 8;
+    // A is a weight: its row is read before waiting for the previous kernel
+    // (up to 8 x 8 columns per thread, i.e. cols <= 16384, held in registers)
+    constexpr int kPre = 8;
+    uint4 pre[kPre];
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+        const long long c = threadIdx.x + (long long)i * blockDim.x;
+        pre[i] = c < n8 ? a8[c] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    griddep_wait();
     float acc[8];
 #pragma unroll
     for (int v = 0; v < 8; ++v) acc[v] = 0.f;
-    const uint4 *a8 = reinterpret_cast<const uint4 *>(A + (long long)k * cols);
-    for (long long c = threadIdx.x; c < cols / 8; c += blockDim.x) {
-        const uint4 w = a8[c];
+    int i = 0;
+    for (long long c = threadIdx.x; c < n8; c += blockDim.x, ++i) {
+        uint4 w;
+        if (i < kPre) {
+            // select the prefetched word without a dynamic register index
+            w = pre[0];
+#pragma unroll
+            for (int t = 1; t < kPre; ++t) if (t == i) w = pre[t];
+        } else {
+            w = a8[c];
+        }
         const float wf[8] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
                              __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u),
                              __uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
@@ -1416,8 +1439,17 @@ hq_status launch_matvec_i8(const int8_t *W, const int8_t *x, const int32_t *mult
 
 hq_status launch_lora_down(const uint16_t *A, const float *x, float *u, int rank, int64_t cols,
                            int n_vec, cudaStream_t stream) {
-    lora_down_kernel<<<(unsigned)rank, 256, 0, stream>>>(A, x, u, rank, (long long)cols, n_vec);
-    cudaError_t e = cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)rank, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, lora_down_kernel, A, x, u, rank, (long long)cols, n_vec);
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "adapter launch: %s", cudaGetErrorString(e));
     return HQ_OK;
 }

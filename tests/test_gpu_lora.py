@@ -133,3 +133,48 @@ def test_lora_full_size_8b_sampled(hq, fmt, rows, cols):
         y_b, T_b = oracle.matvec_rows(fmt, blocks, x, rows, cols, lo, lo + 5)
         d, T_d = oracle.lora_delta(A, B[lo:lo + 5], x, 2.0)
         assert_within(y[:, lo:lo + 5], y_b + d, T_b + T_d, f"{fmt} {rows}x{cols} rows {lo}")
+
+
+def test_lora_chain_in_graph(hq):
+    """Two adapted matvecs chained (the second's x is the first's y), captured
+    in a CUDA graph and replayed with new inputs: the down projection and the
+    matvec both start early under programmatic launch and must still read
+    their inputs only after the kernels that write them."""
+    rows, cols, rank = 4096, 4096, 16
+    stages = []
+    for k, fmt in enumerate(("q8_0", "q4_0")):
+        blocks, A, B, _ = case(fmt, rows, cols, rank, 1, 900 + k)
+        stages.append((fmt, blocks, A, B, dev(blocks), dev(A), dev(B),
+                       torch.empty(rank, dtype=torch.float32, device="cuda")))
+    x0 = torch.empty((1, cols), dtype=torch.float32, device="cuda")
+    ys = [torch.empty((1, rows), dtype=torch.float32, device="cuda") for _ in stages]
+
+    def launch(stream):
+        x = x0
+        for (fmt, _, _, _, Wd, Ad, Bd, ws), y in zip(stages, ys):
+            fn = hq.hq_matvec_q8_0_lora if fmt == "q8_0" else hq.hq_matvec_q4_0_lora
+            fn(Wd, x, Ad, Bd, 0.5, rank, ws, y, rows, cols, 1, stream=stream)
+            x = y
+
+    s = torch.cuda.Stream()
+    g = synthetic.rng(901)
+    x0.copy_(torch.from_numpy(synthetic.activations(g, 1, cols)))
+    with torch.cuda.stream(s):
+        launch(s.cuda_stream)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        launch(torch.cuda.current_stream().cuda_stream)
+    for trial in range(2):
+        x_np = synthetic.activations(g, 1, cols)
+        x0.copy_(torch.from_numpy(x_np))
+        for y in ys:
+            y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        x_in = x_np
+        for (fmt, blocks, A, B, *_), y in zip(stages, ys):
+            y_np = y.cpu().numpy()
+            y_ref, T = reference(fmt, blocks, A, B, x_in, 0.5, rows, cols)
+            assert_within(y_np, y_ref, T, f"trial {trial} {fmt}")
+            x_in = y_np
