@@ -127,6 +127,22 @@ hq_status hq_matvec_q4_0_lora(const void *W, const float *x, const uint16_t *lor
                               float *y, int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
 
 /*
+ * hq_matvec_q8_0_lora_noalloc -- hq_matvec_q8_0_lora without a workspace: the
+ * down projection u = A x is kept in a 2 KB scratch array in the library's
+ * static device memory (one per device, rank <= 64 and n_vec <= 8 always
+ * fit), so the call allocates nothing and takes no memory from the caller.
+ * Arguments, validation, accuracy and kernels are those of
+ * hq_matvec_q8_0_lora.  Because the scratch is shared, calls of this entry
+ * point on one device must not run at the same time (on different streams);
+ * calls on one stream are ordered and safe.
+ * Source: the paper has no counterpart (an allocation-free form of this
+ * library's own QLoRA call).
+ */
+hq_status hq_matvec_q8_0_lora_noalloc(const void *W, const float *x, const uint16_t *lora_A,
+                                      const uint16_t *lora_B, float scale, int rank, float *y,
+                                      int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
+
+/*
  * hq_matvec_i8_requant -- per-output-channel int8 GEMV with gemmlowp requant:
  *   acc = sum_j W[o][j] * x[v][j]  (int32; the caller keeps it in range:
  *         |W|, |x| <= 127 and cols < 133,000 always fit),

@@ -49,6 +49,7 @@ _SIGS = {
     "hq_matvec_i8_requant": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp], _int),
     "hq_matvec_q8_0_lora": ([_vp, _vp, _vp, _vp, ctypes.c_float, _int, _vp, _vp, _i64, _i64, _int, _vp], _int),
     "hq_matvec_q4_0_lora": ([_vp, _vp, _vp, _vp, ctypes.c_float, _int, _vp, _vp, _i64, _i64, _int, _vp], _int),
+    "hq_matvec_q8_0_lora_noalloc": ([_vp, _vp, _vp, _vp, ctypes.c_float, _int, _vp, _i64, _i64, _int, _vp], _int),
     "hq_moe_matvec_q8_0": ([_vp, _vp, _vp, _int, _vp, _i64, _int, _i64, _i64, _int, _vp], _int),
     "hq_quantize_q8_0": ([_vp, _vp, _i64, _i64, _vp], _int),
     "hq_quantize_q4_0": ([_vp, _vp, _i64, _i64, _vp], _int),
@@ -142,6 +143,13 @@ def hq_matvec_q4_0_lora(W, x, lora_A, lora_B, scale: float, rank: int, workspace
     return _check(lib().hq_matvec_q4_0_lora(_addr(W), _addr(x), _addr(lora_A), _addr(lora_B), float(scale),
                                             int(rank), _addr(workspace), _addr(y), rows, cols, n_vec,
                                             _stream(stream)))
+
+
+def hq_matvec_q8_0_lora_noalloc(W, x, lora_A, lora_B, scale: float, rank: int, y, rows: int, cols: int,
+                                n_vec: int, stream=None) -> int:
+    return _check(lib().hq_matvec_q8_0_lora_noalloc(_addr(W), _addr(x), _addr(lora_A), _addr(lora_B),
+                                                    float(scale), int(rank), _addr(y), rows, cols, n_vec,
+                                                    _stream(stream)))
 
 
 def hq_matvec_i8_requant(W, x, mult, shift, y, rows: int, cols: int, n_vec: int, stream=None) -> int:

@@ -17,6 +17,12 @@ namespace hq {
 // The fault word that kernels set instead of trapping (see hq.h).
 __device__ uint32_t g_fault_word;
 
+// Scratch of hq_matvec_q8_0_lora_noalloc: u = A x for the largest adapter
+// (rank 64) at the widest call (8 vectors), 2 KB.  One per device, in the
+// module's static device memory, so that call allocates nothing.
+constexpr int kNoAllocScratchFloats = 64 * 8;
+static __device__ __align__(256) float g_lora_scratch[kNoAllocScratchFloats];
+
 namespace {
 
 thread_local char t_error[512] = "";
@@ -60,6 +66,9 @@ hq_status device_info(DeviceInfo **out) {
         e = cudaGetSymbolAddress(&p, g_fault_word);
         if (e != cudaSuccess) return set_error(HQ_ERR_UNSUPPORTED, "fault word: %s", cudaGetErrorString(e));
         n.fault = static_cast<uint32_t *>(p);
+        e = cudaGetSymbolAddress(&p, g_lora_scratch);
+        if (e != cudaSuccess) return set_error(HQ_ERR_UNSUPPORTED, "adapter scratch: %s", cudaGetErrorString(e));
+        n.lora_scratch = static_cast<float *>(p);
         d = n;
     }
     *out = &d;
@@ -145,6 +154,23 @@ static hq_status matvec_lora(int fmt, const void *W, const float *x, const uint1
     l.rank = rank;
     return finish(fmt == 8 ? launch_matvec_float_q8_0(W, x, y, rows, cols, n_vec, &l, s)
                            : launch_matvec_float_q4_0(W, x, y, rows, cols, n_vec, &l, s));
+}
+
+// hq_matvec_q8_0_lora with u = A x kept in the per-device static scratch
+// instead of a caller's workspace: the call allocates and takes no memory.
+hq_status hq_matvec_q8_0_lora_noalloc(const void *W, const float *x, const uint16_t *lora_A,
+                                      const uint16_t *lora_B, float scale, int rank, float *y, int64_t rows,
+                                      int64_t cols, int n_vec, hq_stream_t stream) {
+    // argument checks first, without touching a device
+    hq_status st = check_float_matvec(W, x, y, rows, cols, n_vec);
+    if (st != HQ_OK) return st;
+    if (!lora_A || !lora_B) return set_error(HQ_ERR_NULL, "lora_A and lora_B must be non-null");
+    if (rank < 1 || rank > 64) return set_error(HQ_ERR_SHAPE, "rank %d not in [1,64]", rank);
+    static_assert(kNoAllocScratchFloats >= 64 * 8, "scratch holds rank 64 x 8 vectors");
+    DeviceInfo *dev = nullptr;
+    st = device_info(&dev);
+    if (st != HQ_OK) return st;
+    return matvec_lora(8, W, x, lora_A, lora_B, scale, rank, dev->lora_scratch, y, rows, cols, n_vec, stream);
 }
 
 hq_status hq_matvec_q8_0_lora(const void *W, const float *x, const uint16_t *lora_A, const uint16_t *lora_B,

@@ -16,6 +16,7 @@ struct DeviceInfo {
     int max_smem_optin = 0;
     int cc_major = 0, cc_minor = 0;
     uint32_t *fault = nullptr;
+    float *lora_scratch = nullptr;   // static device scratch of the allocation-free QLoRA call
 };
 
 hq_status device_info(DeviceInfo **out);            // current device

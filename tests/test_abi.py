@@ -78,6 +78,8 @@ def test_host_validation_before_any_launch(hq):
     assert Lq(fake, fake, fake, fake, float("inf"), 16, fake, fake, 4, 64, 1, 0) == hq.HQ_ERR_SHAPE
     assert Lq(fake, fake, fake + 2, fake, 1.0, 16, fake, fake, 4, 64, 1, 0) == hq.HQ_ERR_ALIGN
     assert L.hq_matvec_q4_0_lora(fake, fake, fake, fake, 1.0, 16, fake, fake, 4, 64, 9, 0) == hq.HQ_ERR_NVEC
+    assert L.hq_matvec_q8_0_lora_noalloc(fake, fake, fake, fake, 1.0, 65, fake, 4, 64, 1, 0) == hq.HQ_ERR_SHAPE
+    assert L.hq_matvec_q8_0_lora_noalloc(fake, fake, 0, fake, 1.0, 16, fake, 4, 64, 1, 0) == hq.HQ_ERR_NULL
     # the wait-timeout self-test bounds its limit before touching a device
     assert L.hq_selftest_wait_timeout(0, 0) == hq.HQ_ERR_SHAPE
     assert L.hq_selftest_wait_timeout(5_000_000_000, 0) == hq.HQ_ERR_SHAPE
