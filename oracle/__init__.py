@@ -73,6 +73,10 @@ def lib() -> ctypes.CDLL:
         L.hqo_bf16_to_float.argtypes = [ctypes.c_uint16]
         L.hqo_bf16_to_float.restype = ctypes.c_float
         L.hqo_lora_delta.argtypes = [_p, _p, _p, ctypes.c_double, _i64, _i64, _i64, _i64, _p, _p]
+        L.hqo_silu.argtypes = [ctypes.c_double]
+        L.hqo_silu.restype = ctypes.c_double
+        L.hqo_swiglu_pairs.argtypes = [_p, _i64, _p]
+        L.hqo_moe_combine.argtypes = [_p, _p, _p, _int, _int, _i64, _p, _p]
         L.hqo_lora_delta.restype = None
         L.hqo_version.restype = _int
         _LIB = L
@@ -271,6 +275,37 @@ def lora_delta(A: np.ndarray, B: np.ndarray, x: np.ndarray, scale: float):
     T = np.empty((n_vec, rows), dtype=np.float64)
     lib().hqo_lora_delta(_ptr(A), _ptr(B), _ptr(x), float(scale), rank, rows, cols, n_vec, _ptr(delta), _ptr(T))
     return delta, T
+
+
+# ---------------------------------------------------------------- MoE epilogues
+
+def silu(z: float) -> float:
+    return float(lib().hqo_silu(float(z)))
+
+
+def swiglu_pairs(y: np.ndarray) -> np.ndarray:
+    """h[..., i] = silu(y[..., 2i]) * y[..., 2i+1] in f64 (interleaved gate/up rows)."""
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    assert y.shape[-1] % 2 == 0
+    h = np.empty(y.shape[:-1] + (y.shape[-1] // 2,), dtype=np.float64)
+    lib().hqo_swiglu_pairs(_ptr(y), h.size, _ptr(h))
+    return h
+
+
+def moe_combine(y: np.ndarray, T, w: np.ndarray):
+    """Router-weighted sum over the slots: y, T f64 [n_vec][n_active][rows],
+    w fp32 [n_vec][n_active].  Returns (out, Tout), f64 [n_vec][rows]."""
+    y = np.ascontiguousarray(y, dtype=np.float64)
+    n_vec, n_active, rows = y.shape
+    w = np.ascontiguousarray(w, dtype=np.float32).reshape(n_vec, n_active)
+    Tp = None
+    if T is not None:
+        T = np.ascontiguousarray(T, dtype=np.float64)
+        Tp = _ptr(T)
+    out = np.empty((n_vec, rows), dtype=np.float64)
+    Tout = np.empty((n_vec, rows), dtype=np.float64)
+    lib().hqo_moe_combine(_ptr(y), Tp, _ptr(w), n_vec, n_active, rows, _ptr(out), _ptr(Tout))
+    return out, Tout
 
 
 def version() -> int:

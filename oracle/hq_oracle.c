@@ -20,7 +20,12 @@
  *          channel symmetric int8 weights, s_w[o] = max|W[o,:]|/127,
  *          Wq = round(W/s_w) in [-127,127]; requant by gemmlowp's
  *          SaturatingRoundingDoublingHighMul then RoundingDivideByPOT to int8,
- *          all integer) and section "Gaps vs the current toy engine", item 3.
+ *          all integer), section "Gaps vs the current toy engine", item 3,
+ *          and section "Architecture" (the feed-forward is SwiGLU(gate, up,
+ *          down)).
+ *   [EPS]  also paragraph "MoE is the cheapest-per-quality tier" (a sparsely
+ *          gated mixture: the output is the gate-weighted sum of the chosen
+ *          experts' outputs).
  *
  * Readings taken where the pages are silent (each one is listed in the design
  * notes): fp16 scale rounded to nearest-even from an fp32 d; q = round(w/d)
@@ -436,6 +441,55 @@ void hqo_lora_delta(const uint16_t *A, const uint16_t *B, const float *x, double
             T[v * rows + i] = fabs(scale) * mag;
         }
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* MoE epilogues.                                                            */
+/*                                                                           */
+/* SwiGLU ([ZEN] "Architecture": every layer's feed-forward is               */
+/* SwiGLU(gate, up, down)).  Reading: the gate is swish-1, silu(z) =         */
+/* z * sigmoid(z) = z / (1 + e^-z), as in the GLU-variant definition of      */
+/* SwiGLU; the hidden value is h_i = silu(gate_i) * up_i.  Reading of the     */
+/* layout: an expert's gate and up matrices are stored as one matrix with    */
+/* their rows interleaved, row 2i = gate row i and row 2i+1 = up row i, so a */
+/* matvec output y gives h_i = silu(y[2i]) * y[2i+1].                        */
+/* ------------------------------------------------------------------------ */
+
+double hqo_silu(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+void hqo_swiglu_pairs(const double *y, int64_t n_pairs, double *h)
+{
+    for (int64_t i = 0; i < n_pairs; ++i) {
+        double gate = y[2 * i], up = y[2 * i + 1];
+        h[i] = hqo_silu(gate) * up;
+    }
+}
+
+/* Router-weighted sum over the slots ([EPS] "MoE is the cheapest-per-      */
+/* quality tier": a sparsely gated mixture reads only its chosen experts;    */
+/* the layer's output is the gate-weighted sum of those experts' outputs).   */
+/* w[t][k] is the router's weight for token t's slot k (an input: the router */
+/* itself is not on the path).  out[t][i] = sum_k w[t][k] * y[t][k][i], k in */
+/* slot order, and Tout = sum_k |w[t][k]| * T[t][k][i], the magnitude the    */
+/* float tolerance is taken against.                                         */
+void hqo_moe_combine(const double *y, const double *T, const float *w, int n_vec, int n_active,
+                     int64_t rows, double *out, double *Tout)
+{
+    for (int t = 0; t < n_vec; ++t)
+        for (int64_t i = 0; i < rows; ++i) {
+            double acc = 0.0, mag = 0.0;
+            for (int k = 0; k < n_active; ++k) {
+                double wk = (double)w[t * n_active + k];
+                int64_t at = ((int64_t)t * n_active + k) * rows + i;
+                acc += wk * y[at];
+                if (T) mag += fabs(wk) * T[at];
+            }
+            out[(int64_t)t * rows + i] = acc;
+            if (Tout) Tout[(int64_t)t * rows + i] = mag;
+        }
 }
 
 int hqo_version(void) { return 1; }

@@ -74,6 +74,40 @@ def lora_delta(A: np.ndarray, B: np.ndarray, x: np.ndarray, scale: float):
     return delta, T
 
 
+# ----------------------------------------------------------- MoE epilogues
+
+def silu_tanh(z):
+    """silu through the identity sigmoid(z) = (1 + tanh(z/2)) / 2, a route that
+    shares no step with the C oracle's z / (1 + e^-z)."""
+    z = np.asarray(z, dtype=np.float64)
+    return z * 0.5 * (1.0 + np.tanh(0.5 * z))
+
+
+def moe_swiglu_q8_0(bank: np.ndarray, ids: np.ndarray, x: np.ndarray, n_experts: int,
+                    rows: int, cols: int) -> np.ndarray:
+    """SwiGLU of an interleaved gate/up bank by brute force: dequantize each
+    chosen expert, split its rows into even (gate) and odd (up), multiply, gate.
+    x: fp32 [n_vec][cols] shared by a token's slots.  Returns f64 [n_vec][n_active][rows/2]."""
+    ids = np.asarray(ids)
+    n_vec, n_active = ids.shape
+    mat = rows * (cols // QK) * 34
+    bank = np.ascontiguousarray(bank, dtype=np.uint8).reshape(-1)
+    h = np.empty((n_vec, n_active, rows // 2))
+    for t in range(n_vec):
+        for k in range(n_active):
+            e = int(ids[t, k])
+            Wd = dequant_q8_0(bank[e * mat:(e + 1) * mat], rows, cols)
+            xv = x[t].astype(np.float64)
+            gate, up = Wd[0::2] @ xv, Wd[1::2] @ xv
+            h[t, k] = silu_tanh(gate) * up
+    return h
+
+
+def moe_combine(y: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """out[t][i] = sum_k w[t][k] y[t][k][i] as one einsum."""
+    return np.einsum("tk,tki->ti", np.asarray(w, dtype=np.float64), np.asarray(y, dtype=np.float64))
+
+
 # ----------------------------------------------------------- independent quantizers
 # A second, vectorised statement of the same readings (fp32 arithmetic), used
 # to cross-check the C quantizers byte for byte.

@@ -41,6 +41,11 @@ MUTANTS = {
     "q4_round_down": ("float t = w[j] / d + 8.5f;", "float t = w[j] / d + 8.0f;"),
     "lora_A_transposed": ("hqo_bf16_to_float(A[k * cols + j])", "hqo_bf16_to_float(A[j * rank + k])"),
     "lora_B_transposed": ("hqo_bf16_to_float(B[i * rank + k])", "hqo_bf16_to_float(B[k * rows + i])"),
+    "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "swiglu_gate_up_swapped": ("double gate = y[2 * i], up = y[2 * i + 1];",
+                               "double gate = y[2 * i + 1], up = y[2 * i];"),
+    "combine_weights_transposed": ("double wk = (double)w[t * n_active + k];",
+                                   "double wk = (double)w[k * n_vec + t];"),
     "lora_scale_dropped": ("delta[v * rows + i] = scale * acc;", "delta[v * rows + i] = acc;"),
     "bf16_shift_15": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
 }
@@ -74,6 +79,10 @@ def _build_mutant(tmp_path, name):
     L.hqo_bf16_to_float.argtypes = [ctypes.c_uint16]
     L.hqo_bf16_to_float.restype = ctypes.c_float
     L.hqo_lora_delta.argtypes = [vp, vp, vp, ctypes.c_double, i64, i64, i64, i64, vp, vp]
+    L.hqo_silu.argtypes = [ctypes.c_double]
+    L.hqo_silu.restype = ctypes.c_double
+    L.hqo_swiglu_pairs.argtypes = [vp, i64, vp]
+    L.hqo_moe_combine.argtypes = [vp, vp, vp, ci, ci, i64, vp, vp]
     return L
 
 
@@ -144,6 +153,20 @@ def _pins_fail(L, golden_dir):
     d_ref, _ = oracle_np.lora_delta(A, B, x, 0.75)
     if not np.allclose(d, d_ref, rtol=1e-12, atol=1e-14):
         failed.append("lora")
+    # MoE epilogues: sigmoid(ln 3) = 3/4, the gate/up pairing, a brute-force combine
+    ln3 = np.log(3.0)
+    if abs(L.hqo_silu(ln3) - 0.75 * ln3) > 1e-15 or abs(L.hqo_silu(-ln3) + 0.25 * ln3) > 1e-15:
+        failed.append("silu")
+    yp = np.array([ln3, 2.0, 0.5, -1.0]); hp = np.empty(2)
+    L.hqo_swiglu_pairs(ptr(yp), 2, ptr(hp))
+    if abs(hp[0] - 1.5 * ln3) > 1e-15:
+        failed.append("swiglu")
+    g = synthetic.rng(321)
+    yc = g.standard_normal((2, 3, 4)); wc = g.standard_normal((2, 3)).astype(np.float32)
+    oc = np.empty((2, 4)); Tc = np.empty((2, 4))
+    L.hqo_moe_combine(ptr(yc), ptr(np.abs(yc)), ptr(wc), 2, 3, 4, ptr(oc), ptr(Tc))
+    if not np.allclose(oc, oracle_np.moe_combine(yc, wc), rtol=1e-13):
+        failed.append("combine")
     return failed
 
 
