@@ -56,6 +56,7 @@ WORKLOADS = {
     "qwen3-0.6b-q8_0": ("dense", "qwen3-0.6b", "q8_0", True),
     "qwen3-0.6b-q8_0-unfused": ("dense", "qwen3-0.6b", "q8_0", False),
     "moe-q8_0": ("moe", "moe-128x8-hidden2048", "q8_0", True),
+    "moe-q8_0-ffn": ("moe", "moe-128x8-hidden2048", "q8_0", True),
     "int8-requant": ("int8", "int8-1024x3072+3072x1024", "i8", False),
     "8b-q8_0-lora": ("dense", "8b-dense", "q8_0", True),
     "8b-q4_0-lora": ("dense", "8b-dense", "q4_0", True),
@@ -65,6 +66,9 @@ WORKLOADS = {
 # projections are the pages' example configuration)
 LORA_RANK = {"8b-q8_0-lora": 16, "8b-q4_0-lora": 16}
 LORA_SCALE = 2.0
+# MoE feed-forward workloads: gate|up with the SwiGLU epilogue (interleaved
+# gate/up rows), down with the router-weighted sum over the slots
+MOE_FFN = {"moe-q8_0-ffn"}
 # MoE decode: a stack of this many layers, each with its own bank of experts
 # (128 x (gate|up 1536x2048 + down 2048x768) Q8_0 = 642 MB per layer)
 MOE_LAYERS = 48
@@ -77,8 +81,9 @@ class Op:
     int8 requant GEMV, with the bytes it reads and writes."""
 
     def __init__(self, kind, name, rows, cols, fmt, n_experts=0, n_active=0, x_per_slot=0, ids=None, label=None,
-                 lora_rank=0):
+                 lora_rank=0, epi=None):
         self.kind, self.name, self.rows, self.cols, self.fmt = kind, name, rows, cols, fmt
+        self.epi = epi                               # MoE epilogue: None, "swiglu" or "combine"
         self.label = label or name                   # the matrix's role, without layer or copy index
         self.lora_rank = lora_rank                   # QLoRA adapter rank (0: none)
         self.n_experts, self.n_active, self.x_per_slot, self.ids = n_experts, n_active, x_per_slot, ids
@@ -87,6 +92,10 @@ class Op:
         return n_vec * (self.n_active if self.x_per_slot else 1) * self.cols
 
     def y_elems(self, n_vec):
+        if self.epi == "swiglu":
+            return n_vec * self.n_active * self.rows // 2     # h = silu(gate) * up
+        if self.epi == "combine":
+            return n_vec * self.rows                         # the weighted sum over the slots
         return n_vec * (self.n_active if self.kind == "moe" else 1) * self.rows
 
     def weight_bytes(self):
@@ -103,6 +112,8 @@ class Op:
         el = 1 if self.kind == "int8" else 4
         extra = self.ids.size * 4 if self.kind == "moe" else 0
         extra += 2 * 4 * self.lora_rank * n_vec                     # u = A x written, then read
+        if self.epi == "combine":
+            extra += 4 * self.ids.size                              # router weights
         return self.weight_bytes() + el * (self.x_elems(n_vec) + self.y_elems(n_vec)) + extra
 
 
@@ -124,10 +135,13 @@ def workload_ops(name, n_vec, shape=None, fmt=None, seed=synthetic.SEED_BASE + 2
         g = synthetic.rng(seed + 7)
         ops = []
         E, A, H, F = synthetic.MOE_N_EXPERTS, synthetic.MOE_N_ACTIVE, synthetic.MOE_HIDDEN, synthetic.MOE_FFN
+        ffn = name in MOE_FFN
         for layer in range(MOE_LAYERS):
             ids = synthetic.expert_ids(g, n_vec, A, E)
-            ops.append(Op("moe", f"gate_up{layer}", 2 * F, H, fmt, E, A, 0, ids, label="gate_up"))
-            ops.append(Op("moe", f"down{layer}", H, F, fmt, E, A, 1, ids, label="down"))
+            ops.append(Op("moe", f"gate_up{layer}", 2 * F, H, fmt, E, A, 0, ids, label="gate_up",
+                          epi="swiglu" if ffn else None))
+            ops.append(Op("moe", f"down{layer}", H, F, fmt, E, A, 1, ids, label="down",
+                          epi="combine" if ffn else None))
         return model, fmt, ops
     ops = []
     for i in range(INT8_COPIES):
@@ -349,6 +363,7 @@ class Step:
         self.ids_all = torch.zeros(max(ni, 4), device=device, dtype=torch.int32)
         self.W, self.x, self.y, self.ids, self.mult, self.shift = [], [], [], [], [], []
         self.lora = []                              # (A, B, workspace) per op, or None
+        self.comb = []                              # router weights per op, or None
         for i, op in enumerate(self.ops):
             self.x.append(self.x_all[xo[i]:xo[i] + op.x_elems(n_vec)])
             self.y.append(self.y_all[yo[i]:yo[i] + op.y_elems(n_vec)])
@@ -373,6 +388,11 @@ class Step:
                 self.lora.append((A, B, ws))
             else:
                 self.lora.append(None)
+            if op.epi == "combine":
+                rw = torch.rand((n_vec, op.n_active), generator=g, device=device).add_(0.05)
+                self.comb.append(rw.div_(rw.sum(dim=1, keepdim=True)))
+            else:
+                self.comb.append(None)
         torch.cuda.synchronize()
         self.weight_bytes = sum(op.weight_bytes() for op in self.ops)
         self.alg_bytes = [op.alg_bytes(n_vec) for op in self.ops]
@@ -434,6 +454,13 @@ class Step:
             elif op.kind == "dense":
                 fn = hq.hq_matvec_q8_0 if op.fmt == "q8_0" else hq.hq_matvec_q4_0
                 fn(self.W[i], self.x[i], self.y[i], op.rows, op.cols, n_vec, stream=stream)
+            elif op.kind == "moe" and op.epi == "swiglu":
+                hq.hq_moe_matvec_q8_0_swiglu(self.W[i], self.ids[i], self.x[i], op.x_per_slot, self.y[i],
+                                             op.n_experts, op.n_active, op.rows, op.cols, n_vec, stream=stream)
+            elif op.kind == "moe" and op.epi == "combine":
+                hq.hq_moe_matvec_q8_0_combine(self.W[i], self.ids[i], self.x[i], op.x_per_slot, self.comb[i],
+                                              self.y[i], op.n_experts, op.n_active, op.rows, op.cols, n_vec,
+                                              stream=stream)
             elif op.kind == "moe":
                 hq.hq_moe_matvec_q8_0(self.W[i], self.ids[i], self.x[i], op.x_per_slot, self.y[i],
                                       op.n_experts, op.n_active, op.rows, op.cols, n_vec, stream=stream)
@@ -518,7 +545,7 @@ class OracleSample:
         self.kind = ops[0].kind
         distinct, keys = [], set()
         for op in ops:
-            k = (op.rows, op.cols, op.x_per_slot)
+            k = (op.rows, op.cols, op.x_per_slot, op.epi)
             if k not in keys:
                 keys.add(k)
                 distinct.append(op)
@@ -547,8 +574,15 @@ class OracleSample:
                 bank = oracle.quantize_q8_0(synthetic.weights(g, U * r, op.cols))
                 ids = remap.reshape(op.ids.shape).astype(np.int32)
                 x = synthetic.activations(g, n_vec * (op.n_active if op.x_per_slot else 1), op.cols)
-                self.calls.append(lambda b=bank, i=ids, x=x, o=op, U=U, r=r:
-                                  oracle.moe_matvec_q8_0(b, i, x, o.x_per_slot, U, o.n_active, r, o.cols, n_vec))
+                moe = (lambda b=bank, i=ids, x=x, o=op, U=U, r=r:
+                       oracle.moe_matvec_q8_0(b, i, x, o.x_per_slot, U, o.n_active, r, o.cols, n_vec))
+                if op.epi == "swiglu":
+                    self.calls.append(lambda f=moe: oracle.swiglu_pairs(f()[0]))
+                elif op.epi == "combine":
+                    rw = synthetic.router_weights(g, n_vec, op.n_active)
+                    self.calls.append(lambda f=moe, w=rw: oracle.moe_combine(*f(), w))
+                else:
+                    self.calls.append(moe)
                 self.pass_bytes += U * weight_bytes("q8_0", r, op.cols)
             else:
                 W = synthetic.weights(g, op.rows, op.cols)
@@ -596,9 +630,11 @@ def describe_workload(args, model, fmt, ops, kind):
         return (f"{model} decode token, {fmt}, n_vec={args.n_vec}: {len(ops)} matvecs "
                 f"(all projections + lm_head){note}{lora}")
     if kind == "moe":
+        ffn = ("; gate|up rows interleaved with the SwiGLU epilogue, down with the router-weighted sum "
+               "over the slots in the same launch" if args.workload in MOE_FFN else "")
         return (f"MoE decode, {MOE_LAYERS} layers x (gate|up 1536x2048 + down 2048x768) per expert, "
                 f"128 experts, 8 active per token drawn uniformly per layer, {fmt}, n_vec={args.n_vec}: "
-                f"{len(ops)} expert-indexed launches")
+                f"{len(ops)} expert-indexed launches{ffn}")
     return (f"int8 GEMV + per-row requant, {INT8_COPIES} distinct copies of each of 1024x3072 and 3072x1024, "
             f"n_vec={args.n_vec}: {len(ops)} launches")
 

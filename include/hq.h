@@ -172,7 +172,8 @@ hq_status hq_matvec_i8_requant(const int8_t *W, const int8_t *x,
  *   y          : fp32 [n_vec][n_active][rows]; y[t][k] = W_bank[ids[t][k]] . x(t,k).
  * Accuracy and the |x| < 2^64 precondition as for hq_matvec_q8_0.
  * Slots that pick the same expert are grouped so that each chosen expert's
- * bytes are streamed once per call.  No router weighting is applied.  An id
+ * bytes are streamed once per call.  No router weighting is applied (the
+ * _combine variant below applies it).  An id
  * outside [0, n_experts) is a precondition violation: its outputs are set to
  * NaN and the device fault word gets HQ_FAULT_EXPERT_ID; nothing traps.
  * Source: "One Native Stack ...", section "The Unified Quant Core" (the MoE
@@ -184,6 +185,51 @@ hq_status hq_moe_matvec_q8_0(const void *W_bank, const int32_t *expert_ids,
                              const float *x, int x_per_slot, float *y,
                              int64_t n_experts, int n_active, int64_t rows, int64_t cols,
                              int n_vec, hq_stream_t stream);
+
+/*
+ * hq_moe_matvec_q8_0_swiglu -- the grouped MoE matvec of an expert bank whose
+ * gate and up matrices are stored as one matrix with their rows interleaved
+ * (row 2i = gate row i, row 2i+1 = up row i; rows = 2 * intermediate, even),
+ * with the SwiGLU gate applied as the outputs are stored:
+ *   h[t][k][i] = silu(g) * u,  g = row 2i . x(t,k),  u = row 2i+1 . x(t,k),
+ *   silu(z) = z / (1 + e^-z).
+ *   h : fp32 [n_vec][n_active][rows / 2], 4-byte aligned; it is the x of the
+ *       down projection (x_per_slot = 1).
+ * Other arguments, grouping and the invalid-id behaviour (NaN outputs, fault
+ * word) as for hq_moe_matvec_q8_0.  Accuracy: g and u are each within the
+ * matvec tolerance e = 1e-3 * sum_j |w_deq * x| + 1e-5 of their exact values;
+ * h is then within 1.1 * e_g * (|u| + e_u) + |silu(g)| * e_u, plus fp32
+ * rounding, of silu(g) * u.
+ * Source: "Blue -- porting zen-nano ...", section "Architecture" (each
+ * layer's feed-forward is SwiGLU(gate, up, down)); the silu gate and the
+ * row interleave are this library's readings.
+ */
+hq_status hq_moe_matvec_q8_0_swiglu(const void *W_bank, const int32_t *expert_ids, const float *x,
+                                    int x_per_slot, float *h, int64_t n_experts, int n_active,
+                                    int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
+
+/*
+ * hq_moe_matvec_q8_0_combine -- the grouped MoE matvec with the router-weighted
+ * sum over each token's slots applied in the same launch:
+ *   y[t][i] = sum_k router_w[t][k] * (W_bank[ids[t][k]] . x(t,k))[i].
+ *   router_w : fp32 [n_vec][n_active], the router's weights for the chosen
+ *              experts (the router itself is the caller's), 4-byte aligned.
+ *   y        : fp32 [n_vec][rows], 4-byte aligned.
+ * A cluster of up to 8 CTAs (as many as one wave of the grid allows) owns
+ * each 32-row tile and splits the tile's expert groups among its CTAs; each
+ * CTA keeps its weighted per-token sums in shared memory and the cluster's
+ * leader adds them over distributed shared memory.  No atomics and no workspace; the summation order is fixed, so y
+ * is the same bits on every run.  A token with an invalid expert id gets
+ * NaN rows (and the fault word HQ_FAULT_EXPERT_ID).  Accuracy: |y - y_ref|
+ * <= 1e-3 * sum_k |router_w[t][k]| * sum_j |w_deq * x| + 1e-5.  Other
+ * arguments as for hq_moe_matvec_q8_0.
+ * Source: "Economical Serving ...", paragraph "MoE is the cheapest-per-quality
+ * tier" (a sparsely gated mixture: the output is the gate-weighted sum of the
+ * chosen experts' outputs).
+ */
+hq_status hq_moe_matvec_q8_0_combine(const void *W_bank, const int32_t *expert_ids, const float *x,
+                                     int x_per_slot, const float *router_w, float *y, int64_t n_experts,
+                                     int n_active, int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
 
 /*
  * Quantizers (the one-off data-preparation step, on the GPU).

@@ -51,6 +51,8 @@ _SIGS = {
     "hq_matvec_q4_0_lora": ([_vp, _vp, _vp, _vp, ctypes.c_float, _int, _vp, _vp, _i64, _i64, _int, _vp], _int),
     "hq_matvec_q8_0_lora_noalloc": ([_vp, _vp, _vp, _vp, ctypes.c_float, _int, _vp, _i64, _i64, _int, _vp], _int),
     "hq_moe_matvec_q8_0": ([_vp, _vp, _vp, _int, _vp, _i64, _int, _i64, _i64, _int, _vp], _int),
+    "hq_moe_matvec_q8_0_swiglu": ([_vp, _vp, _vp, _int, _vp, _i64, _int, _i64, _i64, _int, _vp], _int),
+    "hq_moe_matvec_q8_0_combine": ([_vp, _vp, _vp, _int, _vp, _vp, _i64, _int, _i64, _i64, _int, _vp], _int),
     "hq_quantize_q8_0": ([_vp, _vp, _i64, _i64, _vp], _int),
     "hq_quantize_q4_0": ([_vp, _vp, _i64, _i64, _vp], _int),
     "hq_quantize_i8_rows": ([_vp, _vp, _vp, _i64, _i64, _vp], _int),
@@ -162,6 +164,20 @@ def hq_moe_matvec_q8_0(W_bank, expert_ids, x, x_per_slot: int, y, n_experts: int
     return _check(lib().hq_moe_matvec_q8_0(_addr(W_bank), _addr(expert_ids), _addr(x), int(x_per_slot),
                                            _addr(y), n_experts, n_active, rows, cols, n_vec,
                                            _stream(stream)))
+
+
+def hq_moe_matvec_q8_0_swiglu(W_bank, expert_ids, x, x_per_slot: int, h, n_experts: int, n_active: int,
+                              rows: int, cols: int, n_vec: int, stream=None) -> int:
+    return _check(lib().hq_moe_matvec_q8_0_swiglu(_addr(W_bank), _addr(expert_ids), _addr(x), int(x_per_slot),
+                                                  _addr(h), n_experts, n_active, rows, cols, n_vec,
+                                                  _stream(stream)))
+
+
+def hq_moe_matvec_q8_0_combine(W_bank, expert_ids, x, x_per_slot: int, router_w, y, n_experts: int,
+                               n_active: int, rows: int, cols: int, n_vec: int, stream=None) -> int:
+    return _check(lib().hq_moe_matvec_q8_0_combine(_addr(W_bank), _addr(expert_ids), _addr(x), int(x_per_slot),
+                                                   _addr(router_w), _addr(y), n_experts, n_active, rows, cols,
+                                                   n_vec, _stream(stream)))
 
 
 def hq_quantize_q8_0(W, out, rows: int, cols: int, stream=None) -> int:

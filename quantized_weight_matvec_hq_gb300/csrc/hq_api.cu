@@ -198,9 +198,8 @@ hq_status hq_matvec_i8_requant(const int8_t *W, const int8_t *x, const int32_t *
     return finish(launch_matvec_i8(W, x, mult, shift, y, rows, cols, n_vec, (cudaStream_t)stream));
 }
 
-hq_status hq_moe_matvec_q8_0(const void *W_bank, const int32_t *expert_ids, const float *x,
-                             int x_per_slot, float *y, int64_t n_experts, int n_active, int64_t rows,
-                             int64_t cols, int n_vec, hq_stream_t stream) {
+static hq_status check_moe(const void *W_bank, const int32_t *expert_ids, const float *x, int x_per_slot,
+                           const float *y, int64_t n_experts, int n_active, int64_t rows, int64_t cols, int n_vec) {
     if (!W_bank || !expert_ids || !x || !y) return set_error(HQ_ERR_NULL, "W_bank, expert_ids, x and y must be non-null");
     if (n_vec < 1 || n_vec > 8) return set_error(HQ_ERR_NVEC, "n_vec %d not in [1,8]", n_vec);
     if (n_experts < 1 || n_active < 1 || n_active > n_experts || (long long)n_vec * n_active > 256 ||
@@ -212,8 +211,43 @@ hq_status hq_moe_matvec_q8_0(const void *W_bank, const int32_t *expert_ids, cons
                          (long long)n_experts, n_active, (long long)rows, (long long)cols, x_per_slot);
     if (!aligned(W_bank, 16) || !aligned(x, 16) || !aligned(y, 4) || !aligned(expert_ids, 4))
         return set_error(HQ_ERR_ALIGN, "W_bank and x must be 16-byte aligned");
+    return HQ_OK;
+}
+
+hq_status hq_moe_matvec_q8_0(const void *W_bank, const int32_t *expert_ids, const float *x,
+                             int x_per_slot, float *y, int64_t n_experts, int n_active, int64_t rows,
+                             int64_t cols, int n_vec, hq_stream_t stream) {
+    hq_status st = check_moe(W_bank, expert_ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec);
+    if (st != HQ_OK) return st;
     return finish(launch_moe_q8_0(W_bank, expert_ids, x, x_per_slot, y, n_experts, n_active, rows, cols,
-                                  n_vec, (cudaStream_t)stream));
+                                  n_vec, nullptr, (cudaStream_t)stream));
+}
+
+hq_status hq_moe_matvec_q8_0_swiglu(const void *W_bank, const int32_t *expert_ids, const float *x,
+                                    int x_per_slot, float *h, int64_t n_experts, int n_active, int64_t rows,
+                                    int64_t cols, int n_vec, hq_stream_t stream) {
+    hq_status st = check_moe(W_bank, expert_ids, x, x_per_slot, h, n_experts, n_active, rows, cols, n_vec);
+    if (st != HQ_OK) return st;
+    if (rows % 2 != 0)
+        return set_error(HQ_ERR_SHAPE, "SwiGLU needs interleaved gate/up rows: rows = %lld is odd", (long long)rows);
+    MoeEpi e;
+    e.kind = 1;
+    return finish(launch_moe_q8_0(W_bank, expert_ids, x, x_per_slot, h, n_experts, n_active, rows, cols,
+                                  n_vec, &e, (cudaStream_t)stream));
+}
+
+hq_status hq_moe_matvec_q8_0_combine(const void *W_bank, const int32_t *expert_ids, const float *x,
+                                     int x_per_slot, const float *router_w, float *y, int64_t n_experts,
+                                     int n_active, int64_t rows, int64_t cols, int n_vec, hq_stream_t stream) {
+    hq_status st = check_moe(W_bank, expert_ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec);
+    if (st != HQ_OK) return st;
+    if (!router_w) return set_error(HQ_ERR_NULL, "router_w must be non-null");
+    if (!aligned(router_w, 4)) return set_error(HQ_ERR_ALIGN, "router_w must be 4-byte aligned");
+    MoeEpi e;
+    e.kind = 2;
+    e.router_w = router_w;
+    return finish(launch_moe_q8_0(W_bank, expert_ids, x, x_per_slot, y, n_experts, n_active, rows, cols,
+                                  n_vec, &e, (cudaStream_t)stream));
 }
 
 hq_status hq_quantize_q8_0(const float *W, void *out, int64_t rows, int64_t cols, hq_stream_t stream) {

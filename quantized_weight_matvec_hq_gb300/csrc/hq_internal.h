@@ -39,9 +39,16 @@ hq_status launch_matvec_float_q4_0(const void *W, const float *x, float *y, int6
                                    int64_t cols, int n_vec, const LoraArgs *lora, cudaStream_t stream);
 hq_status launch_lora_down(const uint16_t *A, const float *x, float *u, int rank, int64_t cols,
                            int n_vec, cudaStream_t stream);
+// MoE epilogue of a grouped Q8_0 launch: 0 none; 1 SwiGLU over interleaved
+// gate/up rows (y gets [n_vec][n_active][rows/2]); 2 router-weighted sum over
+// the slots (y gets [n_vec][rows]).
+struct MoeEpi {
+    int kind = 0;
+    const float *router_w = nullptr;    // [n_vec][n_active]
+};
 hq_status launch_moe_q8_0(const void *W_bank, const int32_t *ids, const float *x, int x_per_slot,
                           float *y, int64_t n_experts, int n_active, int64_t rows, int64_t cols,
-                          int n_vec, cudaStream_t stream);
+                          int n_vec, const MoeEpi *epi, cudaStream_t stream);
 hq_status launch_matvec_i8(const int8_t *W, const int8_t *x, const int32_t *mult,
                            const int32_t *shift, int8_t *y, int64_t rows, int64_t cols, int n_vec,
                            cudaStream_t stream);

@@ -585,7 +585,22 @@ struct KArgs {
     const float *lora_u;      //   u = A x, fp32 [n_vec][lora_rank]
     float lora_scale;         //   y += lora_scale * B u
     int lora_rank;
+    int moe_epi;              // MoE epilogue: kEpiNone, kEpiSwiglu or kEpiCombine
+    const float *router_w;    //   combine: router weights [n_vec][n_active]
+    int gsplit;               // combine: CTAs per row tile (a cluster when > 1), over the tile's expert groups
+    int lay_ks;               // gather-buffer slots in the shared-memory layout
 };
+
+// MoE epilogues.  SwiGLU: an expert's gate and up rows are interleaved (row 2i
+// gate i, row 2i+1 up i) and y receives h_i = silu(gate_i) * up_i, [n_vec][n_active][rows/2].
+// Combine: y [n_vec][rows] receives the router-weighted sum over each token's
+// slots.  A cluster of G <= kCombineCluster CTAs owns one row tile (G is as
+// large as one wave of CTAs allows); CTA r takes the expert groups r, r + G,
+// ... and keeps its weighted per-token partial sums in shared memory; the
+// leader adds the CTAs' partials in rank order through distributed shared
+// memory.  No atomics, no workspace, and a fixed summation order.
+constexpr int kEpiNone = 0, kEpiSwiglu = 1, kEpiCombine = 2;
+constexpr int kCombineCluster = 8;
 
 // Consumer warps per CTA for a format and accumulator count.
 template <class P, int NV, int R>
@@ -637,6 +652,28 @@ __device__ __forceinline__ void store_out(const KArgs &a, const MoeTables &mt, i
         const long long p = MOE ? (long long)mt.sorted[mt.gstart[g] + v] : (long long)v;
         if (!MOE && a.lora_rank > 0) val += lora_term(a.lora_B, a.lora_u, a.lora_scale, a.lora_rank, v, row);
         reinterpret_cast<float *>(a.y)[p * a.rows + row] = val;
+    }
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// Entry e of this CTA's own combine partial sums (kept in the gather buffer).
+template <class T>
+__device__ __forceinline__ float csum_own(const T *part, int e) { return reinterpret_cast<const float *>(part)[e]; }
+
+// SwiGLU epilogue of one MoE tile: sums[v * TR + rr] holds the tile's reduced
+// outputs for the group's vector v; rows rr (even) and rr + 1 are a gate/up
+// pair, and h goes to y[pair (token, slot)][tile * TR/2 + rr/2].
+__device__ __forceinline__ void store_swiglu_tile(const KArgs &a, const MoeTables &mt, int g, int tile, int TR,
+                                                  int m, const float *sums, int tid, int nthr) {
+    const long long half = a.rows / 2;
+    for (int e = tid; e < (TR / 2) * m; e += nthr) {
+        const int v = e / (TR / 2), pr = e % (TR / 2);
+        const long long i = (long long)tile * (TR / 2) + pr;
+        if (i >= half) continue;
+        const long long p = mt.sorted[mt.gstart[g] + v];
+        const float gate = sums[v * TR + 2 * pr], up = sums[v * TR + 2 * pr + 1];
+        reinterpret_cast<float *>(a.y)[p * half + i] = silu_f(gate) * up;
     }
 }
 
@@ -702,10 +739,10 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
     const int S = a.stages;
     Red *red = reinterpret_cast<Red *>(smem + L::red_off(S));
     Red *part = reinterpret_cast<Red *>(smem + L::part_off(S));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off(S, a.ksplit));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + L::bar_off(S, a.lay_ks));
     uint64_t *empty = full + S;
     uint64_t *gather_bar = empty + S;           // K split: the leader CTA counts the others' partials
-    int *misc = reinterpret_cast<int *>(smem + L::misc_off(S, a.ksplit));
+    int *misc = reinterpret_cast<int *>(smem + L::misc_off(S, a.lay_ks));
     volatile int *abort_flag = misc;
     const MoeTables mt{misc + 4, misc + 4 + kMaxPairs, misc + 4 + 2 * kMaxPairs,
                        misc + 4 + 3 * kMaxPairs, misc + 1, misc + 4 + 4 * kMaxPairs};
@@ -760,11 +797,12 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
         }
         __syncthreads();
         if (blockIdx.x == 0) {                     // outputs of invalid ids become NaN
-            for (int p = 0; p < P_; ++p) {
+            const long long out_rows = a.moe_epi == kEpiSwiglu ? a.rows / 2 : a.rows;
+            for (int p = 0; p < P_ && a.moe_epi != kEpiCombine; ++p) {   // combine: the leader writes NaN sums
                 const int e = mt.ids[p];
                 if (e >= 0 && e < a.n_experts) continue;
-                for (long long r = threadIdx.x; r < a.rows; r += nthreads)
-                    reinterpret_cast<float *>(a.y)[(long long)p * a.rows + r] = __int_as_float(0x7fc00000);
+                for (long long r = threadIdx.x; r < out_rows; r += nthreads)
+                    reinterpret_cast<float *>(a.y)[(long long)p * out_rows + r] = __int_as_float(0x7fc00000);
             }
         }
     }
@@ -772,11 +810,14 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
 
     const int n_work = MOE ? (*mt.n_groups) * a.num_tiles : a.num_tiles;
     const bool split = a.ksplit > 1;
+    const bool gs = MOE && a.moe_epi == kEpiCombine;   // combine: gsplit CTAs split a row tile's groups
     // every CTA of the cluster has initialised its barriers before any remote access
     if (split) cluster_arrive_relaxed();
-    const int rank = split ? (int)cluster_ctarank() : 0;
-    const int work0 = split ? (int)(blockIdx.x / a.ksplit) : (int)blockIdx.x;
-    const int wstep = split ? max(n_work, 1) : (int)gridDim.x;     // split: one tile per cluster
+    const int rank = (split || (gs && a.gsplit > 1)) ? (int)cluster_ctarank() : 0;
+    // split: one tile per cluster; gs: groups rank, rank + gsplit, ... of the cluster's tile
+    const int work0 = split ? (int)(blockIdx.x / a.ksplit)
+                            : gs ? rank * a.num_tiles + (int)(blockIdx.x / a.gsplit) : (int)blockIdx.x;
+    const int wstep = split ? max(n_work, 1) : gs ? a.gsplit * a.num_tiles : (int)gridDim.x;
     const int k0 = split ? (int)((long long)rank * a.n_chunks / a.ksplit) : 0;
     const int k1 = split ? (int)((long long)(rank + 1) * a.n_chunks / a.ksplit) : a.n_chunks;
     const int nloc = k1 - k0;
@@ -848,6 +889,9 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
     } else {
         // ---------------- consumers
         if (split) cluster_wait();               // the leader's gather buffer and barrier exist
+        float *csum = reinterpret_cast<float *>(part);   // gs: weighted partial sums [n_vec][TR]
+        if (gs)
+            for (int e = threadIdx.x; e < a.n_vec * TR; e += CW * 32) csum[e] = 0.f;
         griddep_wait();                          // y may still be in use by the previous kernel
         uint32_t base = 0;                       // fill number of the current item's first chunk
         for (int work = work0; work < n_work; work += wstep, base += nloc) {
@@ -904,7 +948,19 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 for (int v = 0; v < NV; ++v)
                     red[(warp * NV + v) * TR + lane + 32 * r] = P::finish(acc[r][v]);
             named_barrier(1, CW * 32);
-            for (int e = threadIdx.x; e < TR * m; e += CW * 32) {
+            if (gs) {
+                // one thread per row adds the group's members in order: two slots of a
+                // token may share an expert, so a token's sum has one writer per row
+                for (int rr = threadIdx.x; rr < TR; rr += CW * 32)
+                    for (int v = 0; v < m; ++v) {
+                        Red sum = red[v * TR + rr];
+                        for (int w2 = 1; w2 < CW; ++w2) sum += red[(w2 * NV + v) * TR + rr];
+                        const int p = mt.sorted[mt.gstart[g] + v];
+                        float &c = csum[(p / a.n_active) * TR + rr];
+                        c = fmaf(a.router_w[p], (float)sum, c);
+                    }
+            }
+            for (int e = threadIdx.x; e < TR * m && !gs; e += CW * 32) {
                 const int v = e / TR, rr = e % TR;
                 Red sum = red[v * TR + rr];
                 for (int w2 = 1; w2 < CW; ++w2) sum += red[(w2 * NV + v) * TR + rr];
@@ -914,11 +970,19 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                     const uint32_t slot = smem_u32(&part[((size_t)rank * NV + v) * TR + rr]);
                     if constexpr (std::is_same<Red, int>::value) st_shared_cluster_s32(map_shared_rank(slot, 0), sum);
                     else st_shared_cluster_f32(map_shared_rank(slot, 0), sum);
+                } else if (MOE && a.moe_epi == kEpiSwiglu) {
+                    red[v * TR + rr] = sum;              // paired below (only this thread reads the slot)
                 } else if (row < a.rows) {
                     store_out<P, MOE>(a, mt, g, v, row, sum);
                 }
             }
             named_barrier(1, CW * 32);
+            if constexpr (MOE) {
+                if (!split && a.moe_epi == kEpiSwiglu) {
+                    store_swiglu_tile(a, mt, g, tile, TR, m, reinterpret_cast<const float *>(red), threadIdx.x, CW * 32);
+                    named_barrier(1, CW * 32);           // red is rewritten by the next item
+                }
+            }
             if (split && rank != 0 && threadIdx.x == 0)
                 mbar_arrive_remote(map_shared_rank(smem_u32(gather_bar), 0));
         }
@@ -940,8 +1004,57 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 Red sum = part[(size_t)v * TR + rr];
                 for (int q = 1; q < a.ksplit; ++q) sum += part[((size_t)q * NV + v) * TR + rr];
                 const long long row = (long long)tile * TR + rr;
-                if (row < a.rows) store_out<P, MOE>(a, mt, g, v, row, sum);
+                if (MOE && a.moe_epi == kEpiSwiglu) part[(size_t)v * TR + rr] = sum;    // paired below
+                else if (row < a.rows) store_out<P, MOE>(a, mt, g, v, row, sum);
             }
+            if constexpr (MOE) {
+                if (a.moe_epi == kEpiSwiglu) {
+                    __syncthreads();
+                    store_swiglu_tile(a, mt, g, tile, TR, m, reinterpret_cast<const float *>(part), threadIdx.x, nthreads);
+                }
+            }
+        }
+    }
+
+    if (gs) {
+        // Every CTA of the cluster holds its weighted partial sums; the leader
+        // adds them in rank order through distributed shared memory.  The second
+        // cluster barrier keeps every CTA's shared memory alive until then.
+        __syncwarp();
+        if (a.gsplit > 1) {
+            cluster_arrive_release();
+            cluster_wait();
+        } else {
+            __syncthreads();
+        }
+        if (rank == 0) {
+            const int tile = (int)(blockIdx.x / a.gsplit);
+            const uint32_t base = smem_u32(part);
+            for (int e = threadIdx.x; e < a.n_vec * TR; e += nthreads) {
+                const int t = e / TR, rr = e % TR;
+                const long long row = (long long)tile * TR + rr;
+                if (row >= a.rows) continue;
+                float pv[kCombineCluster];
+#pragma unroll
+                for (int q = 0; q < kCombineCluster; ++q)
+                    pv[q] = q >= a.gsplit ? 0.f
+                          : a.gsplit > 1 ? ld_shared_cluster_f32(map_shared_rank(base + 4u * (uint32_t)e, (uint32_t)q))
+                                         : csum_own(part, e);
+                float acc = pv[0];
+#pragma unroll
+                for (int q = 1; q < kCombineCluster; ++q) if (q < a.gsplit) acc += pv[q];
+                bool valid = true;
+                for (int k = 0; k < a.n_active; ++k) {
+                    const int id = mt.ids[t * a.n_active + k];
+                    valid &= id >= 0 && id < a.n_experts;
+                }
+                reinterpret_cast<float *>(a.y)[(long long)t * a.rows + row] = valid ? acc : __int_as_float(0x7fc00000);
+            }
+        }
+        __syncwarp();
+        if (a.gsplit > 1) {
+            cluster_arrive_release();
+            cluster_wait();
         }
     }
 }
@@ -1119,7 +1232,8 @@ __global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(uint32_t *fau
 namespace {
 
 struct Plan {
-    int stages = 4, ksplit = 1, grid = 1;
+    int stages = 4, ksplit = 1, grid = 1, gsplit = 1, lay_ks = 1;
+    long long slots = 0;
     size_t smem = 0;
 };
 
@@ -1175,7 +1289,7 @@ bool adaptive_ring() {
 // there are too few to fill every CTA slot, K is split across a cluster of up
 // to 8 CTAs, never beyond one wave.
 template <class P, int NV, int R, bool MOE>
-Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_per_thread) {
+Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_per_thread, int gsplit = 0) {
     using L = Layout<P, NV, R, MOE>;
     Plan p;
     const size_t budget = (size_t)dev.max_smem_optin;
@@ -1191,9 +1305,16 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
                                                                           (long long)(budget / p.smem)}));
     const long long slots = (long long)dev.num_sms * per_sm;
     int ks = 1;
-    while (ks < max_ksplit() && n_work * ks * 2 <= slots && n_chunks >= 2 * ks) ks *= 2;
+    p.slots = slots;
+    while (gsplit == 0 && ks < max_ksplit() && n_work * ks * 2 <= slots && n_chunks >= 2 * ks) ks *= 2;
     p.ksplit = ks;
-    if (ks == 1 && P::kComputeBound) {
+    p.gsplit = std::max(gsplit, 1);
+    // gather-buffer slots: the K split's partials, or a combine's own partial sums
+    const int lks = ks > 1 ? ks : (gsplit >= 1 ? 2 : 1);
+    p.lay_ks = lks;
+    if (gsplit >= 1) {
+        p.grid = (int)n_work;                    // n_work counts the CTAs: row tiles x gsplit
+    } else if (ks == 1 && P::kComputeBound) {
         // every slot filled, tiles strided over the CTAs: each SM then holds
         // about the same number of tiles, which is what a decode-bound kernel needs
         p.grid = (int)std::min<long long>(n_work, slots);
@@ -1206,22 +1327,23 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     }
     // the ring takes the shared memory the SM's resident CTAs leave: fewer CTAs
     // per SM get deeper rings, so an SM keeps about the same bytes in flight
-    const long long resident = std::max<long long>(1, (p.grid + dev.num_sms - 1) / dev.num_sms);
+    const long long resident = std::min<long long>(per_sm, std::max<long long>(1, (p.grid + dev.num_sms - 1) / dev.num_sms));
     int st = p.stages;
-    while (st > CW && L::total(st, ks) * resident > budget) st -= CW;     // room for the gather buffer
+    while (st > CW && L::total(st, lks) * resident > budget) st -= CW;    // room for the gather buffer
     if (adaptive_ring())
-        while (st + CW <= 16 && L::total(st + CW, ks) * resident <= budget) st += CW;
+        while (st + CW <= 16 && L::total(st + CW, lks) * resident <= budget) st += CW;
     if (ring_cap()) {
         // a CTA never has more stages than fills: the shared memory it leaves
         // lets the next kernel's CTAs become resident (and start their weight
         // copies) while this one drains
-        const long long items = (ks > 1) ? 1 : (n_work + p.grid - 1) / std::max(p.grid, 1);
+        // (a group split's items are data-dependent: it keeps the full ring)
+        const long long items = (ks > 1) ? 1 : gsplit >= 1 ? 1LL << 30 : (n_work + p.grid - 1) / std::max(p.grid, 1);
         const long long fills = items * ((n_chunks + ks - 1) / ks);
         const long long need = std::max<long long>(CW, (fills + CW - 1) / CW * CW);
         if (need < st) st = (int)need;
     }
     p.stages = st;
-    p.smem = L::total(st, ks);
+    p.smem = L::total(st, lks);
     return p;
 }
 
@@ -1233,6 +1355,40 @@ int kernel_regs() {
         regs = (cudaFuncGetAttributes(&fa, matvec_tma_kernel<P, NV, R, MOE>) == cudaSuccess) ? fa.numRegs : 128;
     }
     return regs;
+}
+
+size_t dev_smem_limit();
+
+// Clusters of G CTAs (smem bytes each) that can be resident at once, from the
+// occupancy calculator; cached per device, kernel, G and size.
+template <class P, int NV, int R, bool MOE>
+long long max_active_clusters(const DeviceInfo &dev, int G, size_t smem) {
+    struct Entry { int device, G; size_t smem; long long n; };
+    static Entry cache[32];
+    static int used = 0;
+    for (int i = 0; i < used; ++i)
+        if (cache[i].device == dev.device && cache[i].G == G && cache[i].smem == smem) return cache[i].n;
+    auto kern = matvec_tma_kernel<P, NV, R, MOE>;
+    long long n = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dev_smem_limit()) == cudaSuccess &&
+        cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) == cudaSuccess) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)G, 1, 1);
+        cfg.blockDim = dim3((unsigned)(32 * (cons_warps<P, NV, R>() + 1)), 1, 1);
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)G;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, kern, &cfg) == cudaSuccess) n = c;
+    }
+    cudaGetLastError();                          // a failed query only means: do not use this G
+    if (used < 32) cache[used++] = Entry{dev.device, G, smem, n};
+    return n;
 }
 
 size_t dev_smem_limit() {
@@ -1262,6 +1418,8 @@ hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
     }
     a.stages = p.stages;
     a.ksplit = p.ksplit;
+    a.gsplit = p.gsplit;
+    a.lay_ks = p.lay_ks;
     if (p.grid <= 0) return HQ_OK;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.grid, 1, 1);
@@ -1273,9 +1431,9 @@ hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
     attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[na].val.programmaticStreamSerializationAllowed = 1;
     ++na;
-    if (p.ksplit > 1) {
+    if (p.ksplit > 1 || p.gsplit > 1) {
         attr[na].id = cudaLaunchAttributeClusterDimension;
-        attr[na].val.clusterDim.x = (unsigned)p.ksplit;
+        attr[na].val.clusterDim.x = (unsigned)std::max(p.ksplit, p.gsplit);
         attr[na].val.clusterDim.y = 1;
         attr[na].val.clusterDim.z = 1;
         ++na;
@@ -1367,7 +1525,7 @@ hq_status dense_dispatch(const DeviceInfo &dev, const void *W, const void *x, vo
 template <int NVMAX>
 hq_status moe_nv(const DeviceInfo &dev, const void *W_bank, const int32_t *ids, const float *x,
                  int x_per_slot, float *y, long long n_experts, int n_active, long long rows,
-                 long long cols, int n_vec, cudaStream_t stream) {
+                 long long cols, int n_vec, const MoeEpi &epi, cudaStream_t stream) {
     using P = PolQ8_0;
     constexpr int R = 1;
     KArgs a = {};
@@ -1387,6 +1545,23 @@ hq_status moe_nv(const DeviceInfo &dev, const void *W_bank, const int32_t *ids, 
     a.n_vec = n_vec;
     a.n_active = n_active;
     a.x_per_slot = x_per_slot;
+    a.moe_epi = epi.kind;
+    a.router_w = epi.router_w;
+    if (epi.kind == kEpiCombine) {
+        // G CTAs per row tile over the tile's expert groups: the largest G
+        // (at most kCombineCluster) whose clusters all fit in one wave, as the
+        // occupancy calculator counts them (clusters are placed within a GPC)
+        const int regs = kernel_regs<P, NVMAX, R, true>();
+        Plan p = make_plan<P, NVMAX, R, true>(dev, a.num_tiles, a.n_chunks, regs, 1);
+        for (int G = kCombineCluster; G > 1; --G) {
+            const Plan q = make_plan<P, NVMAX, R, true>(dev, (long long)a.num_tiles * G, a.n_chunks, regs, G);
+            if (max_active_clusters<P, NVMAX, R, true>(dev, G, q.smem) >= a.num_tiles) {
+                p = q;
+                break;
+            }
+        }
+        return launch_tma<P, NVMAX, R, true>(a, p, stream);
+    }
     // The group count is only known on the device; plan for the most groups the
     // pairs can form (every pair its own expert, at most n_experts of them).
     const long long max_groups = std::min<long long>((long long)n_vec * n_active,
@@ -1474,7 +1649,9 @@ hq_status launch_requant_debug(const int32_t *acc, const int32_t *mult, const in
 #if HQ_PART == 3
 hq_status launch_moe_q8_0(const void *W_bank, const int32_t *ids, const float *x, int x_per_slot,
                           float *y, int64_t n_experts, int n_active, int64_t rows, int64_t cols,
-                          int n_vec, cudaStream_t stream) {
+                          int n_vec, const MoeEpi *epi, cudaStream_t stream) {
+    const MoeEpi none;
+    const MoeEpi &e = epi ? *epi : none;
     DeviceInfo *dev = nullptr;
     hq_status st = device_info(&dev);
     if (st != HQ_OK) return st;
@@ -1483,10 +1660,10 @@ hq_status launch_moe_q8_0(const void *W_bank, const int32_t *ids, const float *x
                          (long long)n_vec * n_active, kMaxPairs);
     if (cols % 256 != 0)
         return set_error(HQ_ERR_SHAPE, "MoE needs cols %% 256 == 0 (cols = %lld)", (long long)cols);
-    if (n_vec <= 1) return moe_nv<1>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, stream);
-    if (n_vec <= 2) return moe_nv<2>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, stream);
-    if (n_vec <= 4) return moe_nv<4>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, stream);
-    return moe_nv<8>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, stream);
+    if (n_vec <= 1) return moe_nv<1>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, e, stream);
+    if (n_vec <= 2) return moe_nv<2>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, e, stream);
+    if (n_vec <= 4) return moe_nv<4>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, e, stream);
+    return moe_nv<8>(*dev, W_bank, ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec, e, stream);
 }
 #endif
 

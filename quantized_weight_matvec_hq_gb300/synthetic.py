@@ -70,6 +70,13 @@ def expert_ids(g: np.random.Generator, n_vec: int, n_active: int, n_experts: int
     return out
 
 
+def router_weights(g: np.random.Generator, n_vec: int, n_active: int) -> np.ndarray:
+    """fp32 [n_vec][n_active]: positive weights summing to 1 per token, as a
+    router hands its chosen experts (exponential draws, normalised)."""
+    w = g.exponential(1.0, size=(n_vec, n_active))
+    return (w / w.sum(axis=1, keepdims=True)).astype(np.float32)
+
+
 def fuse_same_input(layer):
     """Row-concatenate the projections that read the same activation vector:
     q|k|v (the attention input) and gate|up (the MLP input).  The weight bytes

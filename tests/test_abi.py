@@ -67,6 +67,12 @@ def test_host_validation_before_any_launch(hq):
     assert L.hq_moe_matvec_q8_0(fake, fake, fake, 2, fake, 4, 2, 8, 256, 1, 0) == hq.HQ_ERR_SHAPE
     assert L.hq_moe_matvec_q8_0(fake, fake, fake, 0, fake, 64, 64, 8, 256, 8, 0) == hq.HQ_ERR_SHAPE
     assert L.hq_moe_matvec_q8_0(fake, fake, fake, 0, fake, 4, 2, 8, 288, 1, 0) == hq.HQ_ERR_SHAPE
+    # SwiGLU pairs rows: an odd row count is refused; the combine needs its weights and workspaces
+    assert L.hq_moe_matvec_q8_0_swiglu(fake, fake, fake, 0, fake, 4, 2, 9, 256, 1, 0) == hq.HQ_ERR_SHAPE
+    assert L.hq_moe_matvec_q8_0_swiglu(fake, fake, 0, 0, fake, 4, 2, 8, 256, 1, 0) == hq.HQ_ERR_NULL
+    assert L.hq_moe_matvec_q8_0_combine(fake, fake, fake, 1, 0, fake, 4, 2, 8, 256, 1, 0) == hq.HQ_ERR_NULL
+    assert L.hq_moe_matvec_q8_0_combine(fake, fake, fake, 1, fake + 2, fake, 4, 2, 8, 256, 1, 0) == hq.HQ_ERR_ALIGN
+    assert L.hq_moe_matvec_q8_0_combine(fake, fake, fake, 1, fake, fake, 4, 5, 8, 256, 1, 0) == hq.HQ_ERR_SHAPE
     # quantizers
     assert L.hq_quantize_q8_0(fake, fake, 4, 40, 0) == hq.HQ_ERR_SHAPE
     assert L.hq_quantize_q4_0(0, fake, 4, 64, 0) == hq.HQ_ERR_NULL
