@@ -479,9 +479,11 @@ class Step:
         torch.cuda.current_stream().wait_stream(s)
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
+        n0 = self.hq.hq_launch_count()
         with torch.cuda.graph(graph, stream=s):
             self.launch_all(torch.cuda.current_stream().cuda_stream, events)
         torch.cuda.synchronize()
+        self.launches_per_step = self.hq.hq_launch_count() - n0     # kernels the library put in one step
         return graph
 
 
@@ -700,6 +702,7 @@ def main():
 
     step = Step(args.workload, args.n_vec, device, synthetic.SEED_BASE + 2 + rank, args.shape, args.format)
     graph = step.capture()
+    launches_per_step = step.launches_per_step
     events = LaunchEvents(len(ops), _cudart())
     graph_ev = step.capture(events)
 
@@ -808,7 +811,7 @@ def main():
         "per_shape_event_pairs_ms_per_step": round(kernel_ms, 4),
         "e2e": {"value": round(e2e, 2), "unit": "GB/s", "ms_per_step": round(e2e_ms, 5),
                 "h2d_bytes_per_step": int(step.x_bytes + step.ids_bytes), "d2h_bytes_per_step": int(step.y_bytes)},
-        "gpu_launches": sum(2 if op.lora_rank else 1 for op in ops) * args.steps,
+        "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
     }
     # FP32 roof: where the step's flops per byte exceed the ridge of the FP32

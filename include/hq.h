@@ -305,6 +305,14 @@ hq_status hq_device_fault(uint32_t *fault);
  */
 hq_status hq_selftest_wait_timeout(int64_t cycles, hq_stream_t stream);
 
+/*
+ * hq_launch_count -- the number of kernels the library has launched (or
+ * recorded into a stream capture) in this process, on every device: a
+ * monotone host-side counter for callers that account for launches.
+ * Source: none on the pages (introspection of this implementation).
+ */
+uint64_t hq_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

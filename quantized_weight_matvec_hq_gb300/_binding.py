@@ -60,6 +60,7 @@ _SIGS = {
     "hq_requant_i32_debug": ([_vp, _vp, _vp, _vp, _i64, _i64, _vp], _int),
     "hq_device_fault": ([_vp], _int),
     "hq_selftest_wait_timeout": ([_i64, _vp], _int),
+    "hq_launch_count": ([], ctypes.c_uint64),
 }
 
 
@@ -214,3 +215,8 @@ def hq_device_fault() -> int:
     if st != HQ_OK and st != HQ_ERR_DEVICE:
         _check(st)
     return int(v.value)
+
+
+def hq_launch_count() -> int:
+    """Kernels the library has launched or captured so far in this process."""
+    return int(lib().hq_launch_count())

@@ -6,6 +6,7 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include <cmath>
@@ -88,6 +89,9 @@ void *tensor_map_encoder() {
     return g_encoder;
 }
 
+
+std::atomic<uint64_t> g_launches{0};
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 }  // namespace hq
 
 using namespace hq;
@@ -172,6 +176,8 @@ hq_status hq_matvec_q8_0_lora_noalloc(const void *W, const float *x, const uint1
     if (st != HQ_OK) return st;
     return matvec_lora(8, W, x, lora_A, lora_B, scale, rank, dev->lora_scratch, y, rows, cols, n_vec, stream);
 }
+
+uint64_t hq_launch_count(void) { return hq::g_launches.load(std::memory_order_relaxed); }
 
 hq_status hq_matvec_q8_0_lora(const void *W, const float *x, const uint16_t *lora_A, const uint16_t *lora_B,
                               float scale, int rank, float *workspace, float *y, int64_t rows, int64_t cols,

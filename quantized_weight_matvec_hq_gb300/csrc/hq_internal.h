@@ -20,6 +20,7 @@ struct DeviceInfo {
 };
 
 hq_status device_info(DeviceInfo **out);            // current device
+void note_launch();                                 // counts each kernel launch the library makes
 hq_status set_error(hq_status st, const char *fmt, ...);
 void *tensor_map_encoder();                         // PFN_cuTensorMapEncodeTiled
 

@@ -1441,6 +1441,7 @@ hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
     cfg.attrs = attr;
     cfg.numAttrs = na;
     e = cudaLaunchKernelEx(&cfg, kern, a);
+    if (e == cudaSuccess) note_launch();
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "matvec launch: %s", cudaGetErrorString(e));
     return HQ_OK;
 }
@@ -1589,6 +1590,7 @@ hq_status HQ_PART_NAME(launch_matvec_float)(const void *W, const float *x, float
     const unsigned grid = (unsigned)((rows + 7) / 8);
     const LoraArgs none;
     const LoraArgs &l = lora ? *lora : none;
+    note_launch();
     matvec_plain_kernel<FMT><<<grid, 256, 0, stream>>>((const uint8_t *)W, x, y, rows, cols, n_vec,
                                                        l.B, l.u, l.scale, l.rank);
     cudaError_t e = cudaGetLastError();
@@ -1606,6 +1608,7 @@ hq_status launch_matvec_i8(const int8_t *W, const int8_t *x, const int32_t *mult
     if (st != HQ_OK) return st;
     if (cols % 128 == 0)
         return dense_dispatch<PolI8>(*dev, W, x, y, mult, shift, rows, cols, n_vec, nullptr, stream);
+    note_launch();
     matvec_i8_plain_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(W, x, mult, shift, y, rows, cols, n_vec);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "int8 matvec launch: %s", cudaGetErrorString(e));
@@ -1624,12 +1627,14 @@ hq_status launch_lora_down(const uint16_t *A, const float *x, float *u, int rank
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, lora_down_kernel, A, x, u, rank, (long long)cols, n_vec);
+    if (e == cudaSuccess) note_launch();
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "adapter launch: %s", cudaGetErrorString(e));
     return HQ_OK;
 }
 
 hq_status launch_wait_timeout_selftest(uint32_t *fault, int64_t cycles, cudaStream_t stream) {
+    note_launch();
     wait_timeout_selftest_kernel<<<1, 32, 0, stream>>>(fault, (long long)cycles);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "self-test launch: %s", cudaGetErrorString(e));
@@ -1639,6 +1644,7 @@ hq_status launch_wait_timeout_selftest(uint32_t *fault, int64_t cycles, cudaStre
 hq_status launch_requant_debug(const int32_t *acc, const int32_t *mult, const int32_t *shift,
                                int8_t *y, int64_t n, int64_t rows, cudaStream_t stream) {
     const long long blocks = std::min<long long>((n + 255) / 256, 65535);
+    note_launch();
     requant_debug_kernel<<<(unsigned)std::max<long long>(blocks, 1), 256, 0, stream>>>(acc, mult, shift, y, n, rows);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return set_error(HQ_ERR_LAUNCH, "requant launch: %s", cudaGetErrorString(e));

@@ -106,10 +106,12 @@ quantize_i8_rows_kernel(const float *__restrict__ W, int8_t *__restrict__ Wq, fl
 hq_status launch_quantize(int fmt, const float *W, void *out, float *scale, int64_t rows,
                           int64_t cols, cudaStream_t stream) {
     if (fmt == 2) {
+        note_launch();
         quantize_i8_rows_kernel<<<(unsigned)rows, 256, 0, stream>>>(W, (int8_t *)out, scale, cols);
     } else {
         const long long nb = rows * (cols / 32);
         const unsigned grid = (unsigned)((nb + 255) / 256);
+        note_launch();
         if (fmt == 0) quantize_q8_0_kernel<<<grid, 256, 0, stream>>>(W, (uint8_t *)out, nb);
         else quantize_q4_0_kernel<<<grid, 256, 0, stream>>>(W, (uint8_t *)out, nb);
     }

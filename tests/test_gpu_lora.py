@@ -114,6 +114,40 @@ def test_lora_workspace_holds_down_projection_and_is_deterministic(hq):
     assert np.array_equal(y1.view(np.uint32), y2.view(np.uint32))
 
 
+def test_launch_count_per_call(hq):
+    """The library's launch counter: one kernel per plain matvec, two per
+    adapted matvec (the down projection, then the matvec)."""
+    rows, cols, rank = 256, 2048, 16
+    blocks, A, B, x = case("q8_0", rows, cols, rank, 1, 1600)
+    Wd, xd, Ad, Bd = dev(blocks), dev(x), dev(A), dev(B)
+    y = torch.empty((1, rows), dtype=torch.float32, device="cuda")
+    ws = torch.empty(rank, dtype=torch.float32, device="cuda")
+    n0 = hq.hq_launch_count()
+    hq.hq_matvec_q8_0(Wd, xd, y, rows, cols, 1)
+    n1 = hq.hq_launch_count()
+    hq.hq_matvec_q8_0_lora(Wd, xd, Ad, Bd, 1.0, rank, ws, y, rows, cols, 1)
+    n2 = hq.hq_launch_count()
+    torch.cuda.synchronize()
+    assert (n1 - n0, n2 - n1) == (1, 2)
+
+
+def test_lora_one_workspace_for_every_shape(hq):
+    """One workspace of the largest size (rank 64 x 8 vectors) serves calls of
+    different ranks, widths and shapes in turn, on both the TMA kernel and the
+    plain-load kernel (cols % 256 != 0)."""
+    ws = torch.empty(64 * 8, dtype=torch.float32, device="cuda")
+    for k, (fmt, rows, cols, rank, n_vec) in enumerate([("q8_0", 500, 4096, 16, 1), ("q4_0", 257, 3072, 1, 2),
+                                                        ("q8_0", 1000, 2048, 64, 8), ("q4_0", 4096, 14336, 16, 1),
+                                                        ("q8_0", 300, 2336, 8, 3)]):
+        blocks, A, B, x = case(fmt, rows, cols, rank, n_vec, 1500 + k)
+        y = torch.full((n_vec, rows), float("nan"), dtype=torch.float32, device="cuda")
+        fn = hq.hq_matvec_q8_0_lora if fmt == "q8_0" else hq.hq_matvec_q4_0_lora
+        fn(dev(blocks), dev(x), dev(A), dev(B), 1.25, rank, ws, y, rows, cols, n_vec)
+        torch.cuda.synchronize()
+        y_ref, T = reference(fmt, blocks, A, B, x, 1.25, rows, cols)
+        assert_within(y.cpu().numpy(), y_ref, T, f"shared workspace call {k}")
+
+
 @pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
 @pytest.mark.parametrize("rows,cols", [(28672, 4096), (4096, 14336)])
 def test_lora_full_size_8b_sampled(hq, fmt, rows, cols):
