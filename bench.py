@@ -833,8 +833,8 @@ def main():
                                      "peak_source": line["fp32_roof"]["peak_basis"] +
                                      " (derived from unit counts and the sampled clock)"})
     if fmt == "q4_0" and args.n_vec <= 2:
-        line["roofline"]["limiter"] = ("nibble decode issue rate (one lop3 on the ALU pipe, one fadd2 + ffma2 "
-                                       "pair on the FMA pipe per two weights), not HBM")
+        line["roofline"]["limiter"] = ("nibble decode issue rate (one and per weight on the ALU pipe, one ffma2 "
+                                       "per two weights on the FMA pipe), not HBM")
     if not args.no_cpu_baseline and not args.shape:
         gbs, desc, el = OracleSample(args.workload, args.n_vec).timed(args.cpu_budget)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",

@@ -71,15 +71,20 @@ __device__ __forceinline__ float byte_as_float(uint32_t word, int byte) {
     return __uint_as_float(prmt(word, kMagic, 0x7540u | (uint32_t)byte));
 }
 
-// Scale a stage's fp32 x tile ([NV][256]) by 2^64 in place (exact for
-// |x| < 2^64) and return, per lane, the sum of the scaled x of 32-column block
-// lane/4 (every lane of a group of four holds it).  Used by the decodes that
-// read quants as fp32 subnormals: the products quant * 2^-149 * x * 2^64 are
-// then normal numbers, rounded like any fp32 product.
-template <int NV>
-__device__ __forceinline__ void scale_x_tile(uint8_t *xt8, int lane, float (&xs)[NV]) {
+// Scale a stage's fp32 x tile ([NV][256]) in place by 2^64 (exact for
+// |x| < 2^64) and return, per lane, the sum of the 2^64-scaled x of 32-column
+// block lane/4 times XS_MUL (every lane of a group of four holds it).  Used by
+// the decodes that read quants as fp32 subnormals: the products
+// quant * 2^-149 * x * 2^64 are then normal numbers, rounded like any fp32
+// product.  With HI_16 the second half of every block (columns 16..31) is
+// scaled by 2^60 instead, so that a nibble read 4 bits higher in its byte
+// gives a product on the same scale as the low nibble's.
+template <int NV, bool HI_16 = false>
+__device__ __forceinline__ void scale_x_tile(uint8_t *xt8, int lane, float (&xs)[NV], float xs_mul = 1.0f) {
     float4 *xt = reinterpret_cast<float4 *>(xt8);
-    const float2 k64 = make_float2(0x1p64f, 0x1p64f), z = make_float2(0.f, 0.f);
+    const bool hi = HI_16 && (lane & 2);              // this lane's 8 columns are 16..31 of their block
+    const float ks = hi ? 0x1p60f : 0x1p64f;
+    const float2 k64 = make_float2(ks, ks), z = make_float2(0.f, 0.f);
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         float4 a = xt[v * 64 + 2 * lane], b = xt[v * 64 + 2 * lane + 1];
@@ -90,9 +95,10 @@ __device__ __forceinline__ void scale_x_tile(uint8_t *xt8, int lane, float (&xs)
         xt[v * 64 + 2 * lane] = a;
         xt[v * 64 + 2 * lane + 1] = b;
         float t = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
+        if (hi) t *= 16.0f;                           // back to the 2^64 scale (exact)
         t += __shfl_xor_sync(0xffffffffu, t, 1);
         t += __shfl_xor_sync(0xffffffffu, t, 2);
-        xs[v] = t;
+        xs[v] = t * xs_mul;
     }
     __syncwarp();
 }
@@ -303,14 +309,16 @@ __device__ __forceinline__ float nib(uint32_t w, uint32_t magic) {
 
 // Q4_0 nibble decode for one or two vectors, one and per element.  A nibble at bit position
 // p in {0, 4, 8, 12} of a word, masked in place and read as fp32, is the
-// subnormal q * 2^(p-149) -- exactly.  x is first scaled by 2^64 in shared
-// memory (exact for |x| < 2^64), so every product q * x * 2^(p-85) is a
-// normal number, rounded like any fp32 product.  Two adjacent quant bytes
-// always lie in one 16-bit half of a word (the upper half is shifted down),
-// so a pair of low nibbles sits at bits (0, 8) and a pair of high nibbles at
-// bits (4, 12); the four positions are summed apart and joined by exact
-// powers of two once per block, where the offset 8 of every nibble is
-// applied as -8 * d * (the block's x sum).
+// subnormal q * 2^(p-149) -- exactly.  x is first scaled in shared memory by
+// 2^64 in the first half of every block and by 2^60 in the second (exact for
+// |x| < 2^64), so a low nibble (element t, bits p) and a high nibble (element
+// t + 16, bits p + 4) give products on the same scale, q * x * 2^(p-85): every
+// one a normal number, rounded like any fp32 product, summed into one
+// accumulator.  Two adjacent quant bytes always lie in one 16-bit half of a
+// word (the upper half is shifted down), so a pair of elements sits at bits
+// (0, 8) or (4, 12): the accumulator's two lanes carry the scales 2^-85 and
+// 2^-77, joined by exact powers of two once per block, where the offset 8 of
+// every nibble is applied through the block's x sum.
 struct PolQ4_0 {
     static constexpr int kBlockBytes = 18;
     static constexpr int kChunkCols = 256;          // 8 blocks
@@ -332,7 +340,7 @@ struct PolQ4_0 {
 
     template <int NV>
     __device__ __forceinline__ static void prepare(uint8_t *xt8, int lane, float (&xs)[NV]) {
-        if constexpr (scaled_x<NV>()) scale_x_tile<NV>(xt8, lane, xs);
+        if constexpr (scaled_x<NV>()) scale_x_tile<NV, true>(xt8, lane, xs, -0x1p-146f);
     }
 
     template <int NV, int R, int B0, int NB>
@@ -343,13 +351,14 @@ struct PolQ4_0 {
         else consume_magic<NV, R, B0, NB>(wt, xt8, lane, acc);
     }
 
-    // x scaled by 2^64 (prepare), nibbles read as subnormals
+    // x scaled by 2^64 / 2^60 (prepare), nibbles read as subnormals
     template <int NV, int R, int B0, int NB>
     __device__ __forceinline__ static void consume_subnormal(const uint8_t *__restrict__ wt,
                                                              const uint8_t *__restrict__ xt8, int lane,
                                                              Acc (&acc)[R][NV], const float (&xs)[NV]) {
         const float *xt = reinterpret_cast<const float *>(xt8);
-        const float2 kSixteenth = make_float2(0.0625f, 0.0625f);
+        constexpr int NCH = (R * NV >= 4) ? 1 : 2;               // independent FMA chains
+        const float2 kScale = make_float2(0x1p85f, 0x1p77f);    // bits 0/4 carry 2^-85, bits 8/12 2^-77
         const uint4 *rowp[R];
         uint4 c0[R];
 #pragma unroll
@@ -371,13 +380,13 @@ struct PolQ4_0 {
                 sw[r] = win[r][b >> 1];
                 c0[r] = c1;
             }
-            // per row and vector: sums of the low-nibble elements (x: bits 0, y: bits 8)
-            // and of the high-nibble elements (x: bits 4, y: bits 12)
-            float2 slo[R][NV], shi[R][NV];
+            float2 s[R][NV][NCH];
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
-                for (int v = 0; v < NV; ++v) slo[r][v] = shi[r][v] = make_float2(0.f, 0.f);
+                for (int v = 0; v < NV; ++v)
+#pragma unroll
+                    for (int c = 0; c < NCH; ++c) s[r][v][c] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int g = 0; g < 8; ++g) {
                 float4 xv[NV];
@@ -397,25 +406,26 @@ struct PolQ4_0 {
 #pragma unroll
                         for (int v = 0; v < NV; ++v) {
                             const float2 xp = h ? make_float2(xv[v].z, xv[v].w) : make_float2(xv[v].x, xv[v].y);
-                            float2 &sv = high ? shi[r][v] : slo[r][v];
+                            float2 &sv = s[r][v][h % NCH];
                             sv = ffma2(q, xp, sv);
                         }
                     }
                 }
             }
-            float xb[NV];                                       // the block's scaled x sum
+            float xb[NV];                                       // -2^-146 x the block's 2^64-scaled x sum
 #pragma unroll
             for (int v = 0; v < NV; ++v) xb[v] = __shfl_sync(0xffffffffu, xs[v], 4 * b);
 #pragma unroll
             for (int r = 0; r < R; ++r) {
                 const unsigned short hb = (b & 1) ? (unsigned short)(sw[r] >> 16) : (unsigned short)(sw[r] & 0xffffu);
                 const float d = __half2float(__ushort_as_half(hb));
-                const float2 dd = make_float2(d * 0x1p85f, d * 0x1p77f);   // bits 0/4 carry 2^-85, bits 8/12 2^-77
-                const float dbias = d * -0x1p-61f;                          // -8 * d * 2^-64
+                const float2 dd = __fmul2_rn(make_float2(d, d), kScale);
 #pragma unroll
                 for (int v = 0; v < NV; ++v) {
-                    acc[r][v] = ffma2(dd, ffma2(shi[r][v], kSixteenth, slo[r][v]), acc[r][v]);
-                    acc[r][v].x = fmaf(dbias, xb[v], acc[r][v].x);
+                    float2 t = s[r][v][0];
+                    if (NCH == 2) t = fadd2(t, s[r][v][NCH - 1]);
+                    t.x += xb[v];                                // d * 2^85 * xb = -8 * d * (the block's x sum)
+                    acc[r][v] = ffma2(dd, t, acc[r][v]);
                 }
             }
         }
