@@ -115,6 +115,7 @@ struct PolQ8_0 {
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
     static constexpr bool kMayScaleX = true;        // prepare() may rescale the stage's x tile
+    static constexpr bool kRowSplit = false;        // see PolRowSplit
     // one vector: quants read as subnormals (no bias add per pair); more
     // (measured at two: 3688 against 3537 GB/s): through the exponent of 2^23,
     // x as stored
@@ -342,6 +343,7 @@ struct PolQ4_0 {
     static constexpr int kConsWarpsFewAcc = 3;      // n_vec 1 (two rows per lane): three CTAs fit an SM
     static constexpr bool kComputeBound = true;     // decode, not HBM, sets the pace
     static constexpr bool kMayScaleX = true;        // prepare() may rescale the stage's x tile
+    static constexpr bool kRowSplit = false;
     // the subnormal decode (one and per nibble, x scaled by 2^64) pays off at
     // one or two vectors; with more, the per-vector block sums cost more than
     // the bias adds the exponent-OR decode needs
@@ -526,6 +528,7 @@ struct PolI8 {
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
     static constexpr bool kMayScaleX = false;
+    static constexpr bool kRowSplit = false;
     using Acc = int;
     using Red = int;
 
@@ -557,6 +560,19 @@ struct PolI8 {
         }
     }
     __device__ __forceinline__ static Red finish(const Acc &a) { return a; }
+};
+
+// Row-split stages (three or more vectors, float formats).  A stage holds the
+// tile's rows for all CW consumer warps (CW x 32 rows) and one x tile; every
+// warp consumes every stage, each its own 32 rows, and the stage is free once
+// all CW warps have arrived.  The x tile of a K chunk is then loaded and held
+// once per CTA instead of once per warp, which at eight vectors is about half
+// of a warp's shared memory: more warps fit on an SM.  Each row has one owner,
+// so a tile needs no reduction across warps.  The decode must leave x as it
+// is (the decodes of three or more vectors do).
+template <class Base>
+struct PolRowSplit : Base {
+    static constexpr bool kRowSplit = true;
 };
 
 template <class Acc> __device__ __forceinline__ Acc zero_acc();
@@ -629,7 +645,7 @@ __host__ __device__ constexpr int cons_warps() { return (NV * R <= 2) ? P::kCons
 
 template <class P, int NV, int R, bool MOE>
 struct Layout {
-    static constexpr int TR = 32 * R;                                   // rows per tile
+    static constexpr int TR = 32 * R * (P::kRowSplit ? cons_warps<P, NV, R>() : 1);   // rows per tile
     static constexpr int WT = TR * P::kChunkBytes;                      // weight tile bytes
     static constexpr int kAlign = P::kSwizzle ? 1024 : 128;            // TMA destination alignment
     static constexpr int XT = ((NV * P::kChunkCols * P::kXElemBytes + kAlign - 1) / kAlign) * kAlign;
@@ -638,7 +654,9 @@ struct Layout {
     static constexpr size_t kMiscBytes = 16 + (MOE ? 5 * kMaxPairs * 4 : 0);   // abort flag, MoE tables
     // s = ring stages, ks = CTAs per cluster along K (the gather buffer exists only when ks > 1)
     __host__ __device__ static size_t red_off(int s) { return (size_t)s * ST; }
-    __host__ __device__ static size_t part_off(int s) { return red_off(s) + (size_t)cons_warps<P, NV, R>() * TR * NV * 4; }
+    __host__ __device__ static size_t part_off(int s) {
+        return red_off(s) + (size_t)(P::kRowSplit ? 1 : cons_warps<P, NV, R>()) * TR * NV * 4;
+    }
     __host__ __device__ static size_t bar_off(int s, int ks) {
         return part_off(s) + (ks > 1 ? (size_t)ks * TR * NV * 4 : 0);
     }
@@ -739,6 +757,7 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 // four or more consumer warps.
 template <class P, int NV, int R>
 constexpr int ctas_per_sm() {
+    if constexpr (P::kRowSplit) return NV <= 4 ? 5 : 4;
     return cons_warps<P, NV, R>() >= 8 ? 2
          : cons_warps<P, NV, R>() >= 4 ? ((NV * R <= 2) ? 3 : 2)
                                         : ((NV * R <= 2) ? 5 : 3);
@@ -770,12 +789,14 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nthreads = blockDim.x;
-    constexpr int CW = cons_warps<P, NV, R>();      // S % CW == 0 (see make_plan)
+    constexpr int CW = cons_warps<P, NV, R>();      // S % CW == 0 unless rows are split (see make_plan)
+    constexpr bool RS = P::kRowSplit;
+    if constexpr (RS) static_assert(!P::template scaled_x<NV>(), "row-split stages need a decode that leaves x as it is");
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
-            mbar_init(smem_u32(&empty[i]), 1);
+            mbar_init(smem_u32(&empty[i]), P::kRowSplit ? CW : 1);   // row split: every warp frees the stage
         }
         mbar_init(smem_u32(gather_bar), (uint32_t)max(a.ksplit - 1, 1));
         *abort_flag = 0;
@@ -926,8 +947,10 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 for (int v = 0; v < NV; ++v) acc[r][v] = zero_acc<Acc>();
             // fill n lands in stage n % S and belongs to warp n % CW (S is a multiple
             // of CW): each stage is only ever consumed by one warp, in fill order,
-            // so a wait can never mistake a stage's previous phase for its next
-            for (int j = (warp - (int)(base % CW) + CW) % CW; j < nloc; j += CW) {
+            // so a wait can never mistake a stage's previous phase for its next.
+            // Row split: every warp consumes every fill (its own 32 * R rows of
+            // the stage), so each warp waits on every phase of every stage in order.
+            for (int j = RS ? 0 : (warp - (int)(base % CW) + CW) % CW; j < nloc; j += RS ? 1 : CW) {
                 const uint32_t n = base + j;
                 const int s = n % S;
                 mbar_wait(smem_u32(&full[s]), (n / S) & 1, abort_flag, a.fault);
@@ -935,7 +958,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 if constexpr (!MOE) {
                     float xs[NV];
                     P::template prepare<NV>(st + WT, lane, xs);
-                    consume_chunk<P, NV, R>(st, st + WT, lane, acc, xs);
+                    consume_chunk<P, NV, R>(st + (RS ? (size_t)warp * 32 * R * P::kChunkBytes : 0), st + WT, lane, acc, xs);
                 } else {
                     // only the group's m vectors are multiplied
                     switch (m) {
@@ -963,11 +986,13 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
             }
             // reduction of the tile over all consumer warps, in fixed warp order
+            // (row split: each row has one warp, which writes it in place)
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int v = 0; v < NV; ++v)
-                    red[(warp * NV + v) * TR + lane + 32 * r] = P::finish(acc[r][v]);
+                    red[RS ? v * TR + warp * 32 * R + lane + 32 * r : (warp * NV + v) * TR + lane + 32 * r] =
+                        P::finish(acc[r][v]);
             named_barrier(1, CW * 32);
             if (gs) {
                 // one thread per row adds the group's members in order: two slots of a
@@ -975,7 +1000,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 for (int rr = threadIdx.x; rr < TR; rr += CW * 32)
                     for (int v = 0; v < m; ++v) {
                         Red sum = red[v * TR + rr];
-                        for (int w2 = 1; w2 < CW; ++w2) sum += red[(w2 * NV + v) * TR + rr];
+                        for (int w2 = 1; w2 < (RS ? 1 : CW); ++w2) sum += red[(w2 * NV + v) * TR + rr];
                         const int p = mt.sorted[mt.gstart[g] + v];
                         float &c = csum[(p / a.n_active) * TR + rr];
                         c = fmaf(a.router_w[p], (float)sum, c);
@@ -984,7 +1009,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
             for (int e = threadIdx.x; e < TR * m && !gs; e += CW * 32) {
                 const int v = e / TR, rr = e % TR;
                 Red sum = red[v * TR + rr];
-                for (int w2 = 1; w2 < CW; ++w2) sum += red[(w2 * NV + v) * TR + rr];
+                for (int w2 = 1; w2 < (RS ? 1 : CW); ++w2) sum += red[(w2 * NV + v) * TR + rr];
                 const long long row = (long long)tile * TR + rr;
                 if (split) {
                     // this CTA's partial goes to slot `rank` of the leader's gather buffer
@@ -1316,9 +1341,13 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     const size_t budget = (size_t)dev.max_smem_optin;
     const int want = ctas_per_sm<P, NV, R>();
     constexpr int CW = cons_warps<P, NV, R>();
-    // two stages per consumer warp (a double buffer each), more when room allows
-    p.stages = 2 * CW;
-    while (L::total(p.stages + CW, 1) * want <= budget && p.stages < 4 * CW) p.stages += CW;
+    // stages come in multiples of CW (one owner each), or of one when every warp
+    // consumes every stage (row split)
+    constexpr int SQ = P::kRowSplit ? 1 : CW;
+    // two stages per consumer warp (a double buffer each), more when room allows;
+    // row split: two stages for the CTA, more when room allows
+    p.stages = 2 * SQ;
+    while (L::total(p.stages + SQ, 1) * want <= budget && p.stages < 4 * SQ) p.stages += SQ;
     p.smem = L::total(p.stages, 1);
     const int regs = std::max(32, regs_per_thread);
     const long long by_regs = 65536 / (32 * (CW + 1) * ((regs + 7) / 8 * 8));
@@ -1350,9 +1379,10 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     // per SM get deeper rings, so an SM keeps about the same bytes in flight
     const long long resident = std::min<long long>(per_sm, std::max<long long>(1, (p.grid + dev.num_sms - 1) / dev.num_sms));
     int st = p.stages;
-    while (st > CW && L::total(st, lks) * resident > budget) st -= CW;    // room for the gather buffer
+    const int st_min = P::kRowSplit ? 2 : CW;
+    while (st > st_min && L::total(st, lks) * resident > budget) st -= SQ;    // room for the gather buffer
     if (adaptive_ring())
-        while (st + CW <= 16 && L::total(st + CW, lks) * resident <= budget) st += CW;
+        while (st + SQ <= 16 && L::total(st + SQ, lks) * resident <= budget) st += SQ;
     if (ring_cap()) {
         // a CTA never has more stages than fills: the shared memory it leaves
         // lets the next kernel's CTAs become resident (and start their weight
@@ -1360,7 +1390,8 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
         // (a group split's items are data-dependent: it keeps the full ring)
         const long long items = (ks > 1) ? 1 : gsplit >= 1 ? 1LL << 30 : (n_work + p.grid - 1) / std::max(p.grid, 1);
         const long long fills = items * ((n_chunks + ks - 1) / ks);
-        const long long need = std::max<long long>(CW, (fills + CW - 1) / CW * CW);
+        const long long need = P::kRowSplit ? std::max<long long>(2, fills)
+                                            : std::max<long long>(CW, (fills + CW - 1) / CW * CW);
         if (need < st) st = (int)need;
     }
     p.stages = st;
@@ -1481,20 +1512,21 @@ hq_status dense_nv_r(const DeviceInfo &dev, const void *W, const void *x, void *
                      const int32_t *shift, long long rows, long long cols, const LoraArgs *lora,
                      cudaStream_t stream) {
     constexpr bool kI8 = std::is_same<P, PolI8>::value;
+    constexpr int TR = Layout<P, NV, R, false>::TR;             // rows per tile (one TMA box)
     KArgs a = {};
     long long row_bytes;
     hq_status st;
     if constexpr (kI8) {
         row_bytes = cols;
         st = encode_2d(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, W, (uint64_t)cols, (uint64_t)rows,
-                       (uint64_t)row_bytes, P::kBoxInner, 32 * R, true);
+                       (uint64_t)row_bytes, P::kBoxInner, TR, true);
         if (st != HQ_OK) return st;
         st = encode_2d(&a.tmX, CU_TENSOR_MAP_DATA_TYPE_UINT8, x, (uint64_t)cols, (uint64_t)NV,
                        (uint64_t)cols, P::kChunkCols, NV, false);
     } else {
         row_bytes = cols / 32 * P::kBlockBytes;
         st = encode_2d(&a.tmW, CU_TENSOR_MAP_DATA_TYPE_UINT32, W, (uint64_t)(row_bytes / 4),
-                       (uint64_t)rows, (uint64_t)row_bytes, P::kBoxInner, 32 * R, false);
+                       (uint64_t)rows, (uint64_t)row_bytes, P::kBoxInner, TR, false);
         if (st != HQ_OK) return st;
         st = encode_2d(&a.tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, x, (uint64_t)cols, (uint64_t)NV,
                        (uint64_t)cols * 4, P::kChunkCols, NV, false);
@@ -1507,7 +1539,7 @@ hq_status dense_nv_r(const DeviceInfo &dev, const void *W, const void *x, void *
     a.rows = rows;
     a.cols = cols;
     a.n_chunks = (int)(cols / P::kChunkCols);
-    a.num_tiles = (int)((rows + 32 * R - 1) / (32 * R));
+    a.num_tiles = (int)((rows + TR - 1) / TR);
     a.n_vec = NV;
     if (lora && lora->rank > 0) {
         a.lora_B = lora->B;
@@ -1527,6 +1559,12 @@ hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y,
     if constexpr (std::is_same<P, PolQ8_0>::value && NV == 1)
         if (cols <= kShortRowCols)
             return dense_nv_r<PolQ8_0Short, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
+    // Q8_0 at three or more vectors: row-split stages, one x tile per CTA
+    // (8B-shaped token at n_vec 3 / 4 / 8: 2674 / 2255 / 1310 -> 3240 / 2730 /
+    // 1328 GB/s).  Q4_0 keeps one owner per stage: with its 128-row split
+    // stages it measured 1866 / 1605 / 1007 -> 1794 / 1586 / 926 GB/s.
+    if constexpr (NV >= 3 && std::is_same<P, PolQ8_0>::value)
+        return dense_nv_r<PolRowSplit<P>, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
     return dense_nv_r<P, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
 }
 
