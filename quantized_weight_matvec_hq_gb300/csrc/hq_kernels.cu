@@ -758,6 +758,9 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 template <class P, int NV, int R>
 constexpr int ctas_per_sm() {
     if constexpr (P::kRowSplit) return NV <= 4 ? 5 : 4;
+    // Q4_0 at 3-6 vectors: its 96-116 registers leave room for a third CTA
+    // (8B-shaped token n_vec 3 / 4: 1865 / 1606 -> 1939 / 1651 GB/s)
+    if constexpr (std::is_same<P, PolQ4_0>::value) if (NV >= 3 && NV <= 6) return 3;
     return cons_warps<P, NV, R>() >= 8 ? 2
          : cons_warps<P, NV, R>() >= 4 ? ((NV * R <= 2) ? 3 : 2)
                                         : ((NV * R <= 2) ? 5 : 3);
@@ -1560,9 +1563,10 @@ hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y,
         if (cols <= kShortRowCols)
             return dense_nv_r<PolQ8_0Short, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
     // Q8_0 at three or more vectors: row-split stages, one x tile per CTA
-    // (8B-shaped token at n_vec 3 / 4 / 8: 2674 / 2255 / 1310 -> 3240 / 2730 /
-    // 1328 GB/s).  Q4_0 keeps one owner per stage: with its 128-row split
-    // stages it measured 1866 / 1605 / 1007 -> 1794 / 1586 / 926 GB/s.
+    // (8B-shaped token at n_vec 3 / 4 / 6 / 8: 2674 / 2255 / 1654 / 1310 ->
+    // 3240 / 2730 / 1720 / 1328 GB/s; at n_vec 2 no gain).  Q4_0 keeps one
+    // owner per stage: with its 128-row split stages it measured 1866 / 1605 /
+    // 1007 -> 1794 / 1586 / 926 GB/s at n_vec 3 / 4 / 8.
     if constexpr (NV >= 3 && std::is_same<P, PolQ8_0>::value)
         return dense_nv_r<PolRowSplit<P>, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
     return dense_nv_r<P, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
