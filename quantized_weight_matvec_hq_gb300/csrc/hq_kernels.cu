@@ -340,7 +340,7 @@ struct PolQ4_0 {
     static constexpr int kUnits = 8;
     static constexpr bool kSwizzle = false;
     static constexpr int kConsWarps = 4;            // nibble decode is ALU-heavy: more warps hide its latency
-    static constexpr int kConsWarpsFewAcc = 3;      // n_vec 1 (two rows per lane): three CTAs fit an SM
+    static constexpr int kConsWarpsFewAcc = 4;      // n_vec 1 (two rows per lane; see make_plan's ring)
     static constexpr bool kComputeBound = true;     // decode, not HBM, sets the pace
     static constexpr bool kMayScaleX = true;        // prepare() may rescale the stage's x tile
     static constexpr bool kRowSplit = false;
@@ -1349,7 +1349,13 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     constexpr int SQ = P::kRowSplit ? 1 : CW;
     // two stages per consumer warp (a double buffer each), more when room allows;
     // row split: two stages for the CTA, more when room allows
-    p.stages = 2 * SQ;
+    // Q4_0 at one vector starts from one stage per warp: with four consumer
+    // warps the ring then leaves room for 3 CTAs per SM (2 with two stages per
+    // warp); the ring still grows below when fewer CTAs are resident.  8B-shaped
+    // Q4_0 token: 3154 GB/s with three warps and two stages each, 3411 with
+    // three warps and one, 3568 with four warps and one.
+    constexpr int kSpw = (std::is_same<P, PolQ4_0>::value && NV == 1) ? 1 : 2;
+    p.stages = kSpw * SQ;
     while (L::total(p.stages + SQ, 1) * want <= budget && p.stages < 4 * SQ) p.stages += SQ;
     p.smem = L::total(p.stages, 1);
     const int regs = std::max(32, regs_per_thread);
