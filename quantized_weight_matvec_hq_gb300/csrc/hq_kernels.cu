@@ -301,6 +301,12 @@ struct PolQ8_0Short : PolQ8_0 {
 };
 constexpr long long kShortRowCols = 3072;
 
+// The expert-indexed kernel at one vector: three consumer warps per CTA (with a
+// ring of one stage per warp, see make_plan).
+struct PolQ8_0Moe : PolQ8_0 {
+    static constexpr int kConsWarpsFewAcc = 3;
+};
+
 // Q4_0 nibble decode for three or more vectors, one and-or per element: a
 // nibble at bit p in {0, 4, 8, 12}, masked in place and ORed into the
 // exponent of 2^23, is the fp32 value 2^23 + q * 2^p (exact: the mantissa has
@@ -1353,8 +1359,10 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     // warps the ring then leaves room for 3 CTAs per SM (2 with two stages per
     // warp); the ring still grows below when fewer CTAs are resident.  8B-shaped
     // Q4_0 token: 3154 GB/s with three warps and two stages each, 3411 with
-    // three warps and one, 3568 with four warps and one.
-    constexpr int kSpw = (std::is_same<P, PolQ4_0>::value && NV == 1) ? 1 : 2;
+    // three warps and one, 3568 with four warps and one.  The MoE kernel at one
+    // vector does the same with three warps (48-layer step 2399 -> 2526 GB/s);
+    // the dense Q8_0 kernel does not (8B token 5186 -> 4607 GB/s).
+    constexpr int kSpw = ((std::is_same<P, PolQ4_0>::value || std::is_same<P, PolQ8_0Moe>::value) && NV == 1) ? 1 : 2;
     p.stages = kSpw * SQ;
     while (L::total(p.stages + SQ, 1) * want <= budget && p.stages < 4 * SQ) p.stages += SQ;
     p.smem = L::total(p.stages, 1);
@@ -1599,7 +1607,7 @@ template <int NVMAX>
 hq_status moe_nv(const DeviceInfo &dev, const void *W_bank, const int32_t *ids, const float *x,
                  int x_per_slot, float *y, long long n_experts, int n_active, long long rows,
                  long long cols, int n_vec, const MoeEpi &epi, cudaStream_t stream) {
-    using P = PolQ8_0;
+    using P = typename std::conditional<NVMAX == 1, PolQ8_0Moe, PolQ8_0>::type;
     constexpr int R = 1;
     KArgs a = {};
     const long long row_bytes = cols / 32 * P::kBlockBytes;
