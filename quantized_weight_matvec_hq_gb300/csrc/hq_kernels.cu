@@ -306,6 +306,11 @@ constexpr long long kShortRowCols = 3072;
 struct PolQ8_0Moe : PolQ8_0 {
     static constexpr int kConsWarpsFewAcc = 3;
 };
+// Q8_0 at two vectors: three consumer warps per CTA, with a ring of one
+// stage per warp (8B-shaped token 3714 -> 3819 GB/s).
+struct PolQ8_0Two : PolQ8_0 {
+    static constexpr int kConsWarpsFewAcc = 3;
+};
 
 // Q4_0 nibble decode for three or more vectors, one and-or per element: a
 // nibble at bit p in {0, 4, 8, 12}, masked in place and ORed into the
@@ -1360,9 +1365,12 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     // warp); the ring still grows below when fewer CTAs are resident.  8B-shaped
     // Q4_0 token: 3154 GB/s with three warps and two stages each, 3411 with
     // three warps and one, 3568 with four warps and one.  The MoE kernel at one
-    // vector does the same with three warps (48-layer step 2399 -> 2526 GB/s);
-    // the dense Q8_0 kernel does not (8B token 5186 -> 4607 GB/s).
-    constexpr int kSpw = ((std::is_same<P, PolQ4_0>::value || std::is_same<P, PolQ8_0Moe>::value) && NV == 1) ? 1 : 2;
+    // vector does the same with three warps (48-layer step 2399 -> 2526 GB/s),
+    // and so does the dense Q8_0 kernel at two vectors (PolQ8_0Two); the dense
+    // Q8_0 kernel at one vector does not (8B token 5186 -> 4607 GB/s), nor the
+    // MoE kernel at four vectors (2696 -> 2579 GB/s).
+    constexpr int kSpw = (((std::is_same<P, PolQ4_0>::value || std::is_same<P, PolQ8_0Moe>::value) && NV == 1) ||
+                          (std::is_same<P, PolQ8_0Two>::value && NV == 2)) ? 1 : 2;
     p.stages = kSpw * SQ;
     while (L::total(p.stages + SQ, 1) * want <= budget && p.stages < 4 * SQ) p.stages += SQ;
     p.smem = L::total(p.stages, 1);
@@ -1581,6 +1589,8 @@ hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y,
     // 3240 / 2730 / 1720 / 1328 GB/s; at n_vec 2 no gain).  Q4_0 keeps one
     // owner per stage: with its 128-row split stages it measured 1866 / 1605 /
     // 1007 -> 1794 / 1586 / 926 GB/s at n_vec 3 / 4 / 8.
+    if constexpr (NV == 2 && std::is_same<P, PolQ8_0>::value)
+        return dense_nv_r<PolQ8_0Two, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
     if constexpr (NV >= 3 && std::is_same<P, PolQ8_0>::value)
         return dense_nv_r<PolRowSplit<P>, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
     return dense_nv_r<P, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);

@@ -372,3 +372,38 @@ def test_moe_invalid_id_sets_fault_and_nan(hq):
     y_ref, T = oracle.moe_matvec_q8_0(bank, ok, x, False, n_experts, n_active, rows, cols, n_vec)
     assert_within(y[:, 0], y_ref[:, 0], T[:, 0], "valid slots beside invalid ones")
     assert hq.hq_device_fault() == 0
+
+
+# ---------------------------------------------------------------- launch-policy boundaries
+
+@pytest.mark.parametrize("rows,cols,n_vec", [
+    (97, 3072, 1),      # Q8_0 short rows (four consumer warps), ragged last tile
+    (97, 3328, 1),      # one K chunk past the short-row limit: two warps, K split over a cluster
+    (1000, 1024, 1),    # short rows, many tiles
+    (4100, 4096, 3),    # row-split stages (64-row tiles), ragged last tile
+    (4100, 4096, 6),
+    (333, 14336, 7),    # row-split stages with a K split over a cluster
+])
+def test_q8_0_launch_policy_boundaries(hq, rows, cols, n_vec):
+    """Each Q8_0 launch policy at and around its switch point (rows of at most
+    3072 columns at one vector; row-split stages at three or more vectors),
+    element by element against the oracle."""
+    g = synthetic.rng(4242 + rows + cols + n_vec)
+    blocks = quant("q8_0", synthetic.weights(g, rows, cols))
+    x = synthetic.activations(g, n_vec, cols)
+    y_ref, T = oracle.matvec("q8_0", blocks, x, rows, cols)
+    y = gpu_matvec(hq, "q8_0", blocks, x, rows, cols)
+    assert_within(y, y_ref, T, f"q8_0 {rows}x{cols} n_vec={n_vec}")
+
+
+@pytest.mark.parametrize("rows,cols,n_vec", [(4100, 4096, 1), (333, 14336, 1), (4100, 4096, 5)])
+def test_q4_0_launch_policy_boundaries(hq, rows, cols, n_vec):
+    """Q4_0 at one vector (four consumer warps, a ring of one stage per warp)
+    and at five vectors (three CTAs per SM), ragged last tiles, against the
+    oracle."""
+    g = synthetic.rng(5151 + rows + cols + n_vec)
+    blocks = quant("q4_0", synthetic.weights(g, rows, cols))
+    x = synthetic.activations(g, n_vec, cols)
+    y_ref, T = oracle.matvec("q4_0", blocks, x, rows, cols)
+    y = gpu_matvec(hq, "q4_0", blocks, x, rows, cols)
+    assert_within(y, y_ref, T, f"q4_0 {rows}x{cols} n_vec={n_vec}")
