@@ -756,7 +756,9 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 // owns the tile's 32*R rows (R per lane); S is a multiple of CW, so every
 // stage has one owner.  A tile ends with a fixed-order reduction over the CW
 // warps; with a K split, the CTAs of a cluster then combine their partials
-// through DSMEM.
+// through DSMEM.  With row-split stages (PolRowSplit) a tile is CW*32*R rows,
+// every warp consumes every fill (its own 32*R rows, one shared x tile), and
+// the stage is freed by all CW warps; rows need no reduction across warps.
 //
 // Programmatic dependent launch: the kernel lets the next one in the stream
 // start as soon as it is resident, issues the weight copies of its first
