@@ -127,14 +127,25 @@ hq_status hq_matvec_q4_0_lora(const void *W, const float *x, const uint16_t *lor
                               float *y, int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
 
 /*
- * hq_matvec_q8_0_lora_noalloc -- hq_matvec_q8_0_lora without a workspace: the
- * down projection u = A x is kept in a 2 KB scratch array in the library's
- * static device memory (one per device, rank <= 64 and n_vec <= 8 always
- * fit), so the call allocates nothing and takes no memory from the caller.
- * Arguments, validation, accuracy and kernels are those of
- * hq_matvec_q8_0_lora.  Because the scratch is shared, calls of this entry
- * point on one device must not run at the same time (on different streams);
- * calls on one stream are ordered and safe.
+ * hq_matvec_q8_0_lora_noalloc -- hq_matvec_q8_0_lora without a workspace, for
+ * callers that cannot allocate device memory.  Examples are code inside an
+ * engine that hands all device memory to its own pre-sized pool, and a hot
+ * path that must not call cudaMalloc / cudaFree, which may synchronize the
+ * device.  Such a caller can pass no workspace for u = A x.
+ *   Scratch: u lives in one file-scope array of 2 KB in the library's static
+ *   device memory (64 x 8 fp32: the largest rank times the largest n_vec).
+ *   Every GPU that loads the library holds it until the process exits.  A call
+ *   with rank > 64 (or n_vec > 8) is rejected with HQ_ERR_SHAPE before any
+ *   launch.  The call itself allocates nothing: no cudaMalloc, no cudaFree, no
+ *   allocating library routine.
+ *   Set-up: the library's first call on a device (this entry point or any
+ *   other) looks up the scratch's device address with that device current.
+ *   Make that first call before any stream capture.
+ *   Sharing: every call on a device uses the same array, and nothing in it
+ *   needs to start at zero (each call writes all of u before reading it).
+ *   Calls of this entry point that overlap on the GPU (on different streams of
+ *   one device) race on the array.  Calls on one stream are ordered and safe.
+ * Arguments, validation, accuracy and kernels are those of hq_matvec_q8_0_lora.
  * Source: the paper has no counterpart (an allocation-free form of this
  * library's own QLoRA call).
  */

@@ -18,9 +18,12 @@ namespace hq {
 // The fault word that kernels set instead of trapping (see hq.h).
 __device__ uint32_t g_fault_word;
 
-// Scratch of hq_matvec_q8_0_lora_noalloc: u = A x for the largest adapter
-// (rank 64) at the widest call (8 vectors), 2 KB.  One per device, in the
-// module's static device memory, so that call allocates nothing.
+// Scratch of hq_matvec_q8_0_lora_noalloc, the QLoRA call for callers that
+// cannot allocate device memory: u = A x for the largest adapter (rank 64) at
+// the widest call (8 vectors), 2 KB.  One per device, in the module's static
+// device memory, held until the process exits.  In host code the symbol is a
+// host-side stand-in, so device_info() looks up its device address once per
+// device (with that device current) and launches use that address.
 constexpr int kNoAllocScratchFloats = 64 * 8;
 static __device__ __align__(256) float g_lora_scratch[kNoAllocScratchFloats];
 
@@ -162,6 +165,7 @@ static hq_status matvec_lora(int fmt, const void *W, const float *x, const uint1
 
 // hq_matvec_q8_0_lora with u = A x kept in the per-device static scratch
 // instead of a caller's workspace: the call allocates and takes no memory.
+// Calls that overlap on one device race on the scratch (see hq.h).
 hq_status hq_matvec_q8_0_lora_noalloc(const void *W, const float *x, const uint16_t *lora_A,
                                       const uint16_t *lora_B, float scale, int rank, float *y, int64_t rows,
                                       int64_t cols, int n_vec, hq_stream_t stream) {
