@@ -324,6 +324,27 @@ hq_status hq_selftest_wait_timeout(int64_t cycles, hq_stream_t stream);
  */
 uint64_t hq_launch_count(void);
 
+/*
+ * hq_debug_plan -- test-only: the launch geometry the library would choose for
+ * a dense matvec of `rows` x `cols` at `n_vec` vectors, on a device with
+ * `num_sms` SMs and `smem_optin` bytes of opt-in shared memory per CTA, for a
+ * kernel of `regs` registers per thread.  Pure host arithmetic: no device is
+ * touched, so it also runs on a machine without a GPU.
+ *   fmt : 8 (Q8_0), 4 (Q4_0) or 1 (int8).  cols : a multiple of 256 (int8:
+ *         128), the shapes the TMA-staged kernel serves.
+ *   out : int64 [out_len >= HQ_PLAN_FIELDS], caller-owned host memory,
+ *         filled with { policy (0 one owner per stage, 1 Q8_0 short rows,
+ *         2 Q8_0 two vectors, 3 row-split stages), consumer warps per CTA,
+ *         rows per tile, grid (CTAs), K split (CTAs per cluster), ring stages,
+ *         dynamic shared memory bytes, CTAs per SM of the launch bound,
+ *         CTA slots (SMs x CTAs per SM the plan assumed), row tiles }.
+ * Errors: HQ_ERR_NULL, HQ_ERR_SHAPE, HQ_ERR_NVEC, HQ_ERR_UNSUPPORTED (fmt).
+ * Source: none on the pages (introspection of this implementation).
+ */
+#define HQ_PLAN_FIELDS 10
+hq_status hq_debug_plan(int fmt, int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin, int regs,
+                        int64_t *out, int out_len);
+
 #ifdef __cplusplus
 }
 #endif

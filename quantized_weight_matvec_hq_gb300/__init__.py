@@ -20,6 +20,6 @@ from ._binding import (  # noqa: F401
     hq_moe_matvec_q8_0_swiglu, hq_moe_matvec_q8_0_combine,
     hq_matvec_q8_0_lora, hq_matvec_q4_0_lora, hq_matvec_q8_0_lora_noalloc,
     hq_quantize_q8_0, hq_quantize_q4_0, hq_quantize_i8_rows, hq_requant_params,
-    hq_requant_i32_debug, hq_device_fault, hq_selftest_wait_timeout, hq_launch_count,
+    hq_requant_i32_debug, hq_device_fault, hq_selftest_wait_timeout, hq_launch_count, hq_debug_plan,
     Q8_0_BLOCK_BYTES, Q4_0_BLOCK_BYTES, QK, row_bytes,
 )

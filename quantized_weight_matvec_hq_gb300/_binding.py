@@ -61,6 +61,7 @@ _SIGS = {
     "hq_device_fault": ([_vp], _int),
     "hq_selftest_wait_timeout": ([_i64, _vp], _int),
     "hq_launch_count": ([], ctypes.c_uint64),
+    "hq_debug_plan": ([_int, _int, _i64, _i64, _int, _int, _int, ctypes.POINTER(ctypes.c_int64), _int], _int),
 }
 
 
@@ -215,6 +216,18 @@ def hq_device_fault() -> int:
     if st != HQ_OK and st != HQ_ERR_DEVICE:
         _check(st)
     return int(v.value)
+
+
+PLAN_FIELDS = ("policy", "cons_warps", "tile_rows", "grid", "ksplit", "stages", "smem", "ctas_per_sm",
+               "slots", "tiles")
+
+
+def hq_debug_plan(fmt: int, n_vec: int, rows: int, cols: int, num_sms: int, smem_optin: int, regs: int) -> dict:
+    """HOST function (test-only): the launch geometry the library would choose, as a dict."""
+    out = (ctypes.c_int64 * len(PLAN_FIELDS))()
+    _check(lib().hq_debug_plan(int(fmt), int(n_vec), int(rows), int(cols), int(num_sms), int(smem_optin),
+                               int(regs), out, len(PLAN_FIELDS)))
+    return dict(zip(PLAN_FIELDS, (int(v) for v in out)))
 
 
 def hq_launch_count() -> int:

@@ -183,6 +183,27 @@ hq_status hq_matvec_q8_0_lora_noalloc(const void *W, const float *x, const uint1
 
 uint64_t hq_launch_count(void) { return hq::g_launches.load(std::memory_order_relaxed); }
 
+hq_status hq_debug_plan(int fmt, int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin, int regs,
+                        int64_t *out, int out_len) {
+    if (!out) return set_error(HQ_ERR_NULL, "out must be non-null");
+    if (out_len < HQ_PLAN_FIELDS) return set_error(HQ_ERR_SHAPE, "out needs %d entries", HQ_PLAN_FIELDS);
+    if (n_vec < 1 || n_vec > 8) return set_error(HQ_ERR_NVEC, "n_vec %d not in [1,8]", n_vec);
+    if (rows < 1 || rows > 0x7fffffffLL) return set_error(HQ_ERR_SHAPE, "rows %lld out of range", (long long)rows);
+    if (num_sms < 1 || smem_optin < 1024 || regs < 1 || regs > 255)
+        return set_error(HQ_ERR_SHAPE, "device description out of range (num_sms %d, smem %d, regs %d)", num_sms,
+                         smem_optin, regs);
+    const int64_t chunk = fmt == 1 ? 128 : 256;
+    if (cols < chunk || cols % chunk != 0 || cols > (1LL << 31))
+        return set_error(HQ_ERR_SHAPE, "cols %lld: the staged kernel needs a multiple of %lld", (long long)cols,
+                         (long long)chunk);
+    switch (fmt) {
+        case 8: return debug_plan_float_q8_0(n_vec, rows, cols, num_sms, smem_optin, regs, out);
+        case 4: return debug_plan_float_q4_0(n_vec, rows, cols, num_sms, smem_optin, regs, out);
+        case 1: return debug_plan_i8(n_vec, rows, cols, num_sms, smem_optin, regs, out);
+        default: return set_error(HQ_ERR_UNSUPPORTED, "fmt %d: 8 (Q8_0), 4 (Q4_0) or 1 (int8)", fmt);
+    }
+}
+
 hq_status hq_matvec_q8_0_lora(const void *W, const float *x, const uint16_t *lora_A, const uint16_t *lora_B,
                               float scale, int rank, float *workspace, float *y, int64_t rows, int64_t cols,
                               int n_vec, hq_stream_t stream) {

@@ -58,5 +58,11 @@ hq_status launch_requant_debug(const int32_t *acc, const int32_t *mult, const in
                                int8_t *y, int64_t n, int64_t rows, cudaStream_t stream);
 hq_status launch_quantize(int fmt, const float *W, void *out, float *scale, int64_t rows,
                           int64_t cols, cudaStream_t stream);
+// Test-only plan queries (no device touched): see hq_debug_plan in hq.h.
+hq_status debug_plan_float_q8_0(int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin, int regs,
+                                int64_t *out);
+hq_status debug_plan_float_q4_0(int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin, int regs,
+                                int64_t *out);
+hq_status debug_plan_i8(int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin, int regs, int64_t *out);
 
 }  // namespace hq

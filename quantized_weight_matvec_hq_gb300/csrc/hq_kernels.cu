@@ -1578,24 +1578,87 @@ hq_status dense_nv_r(const DeviceInfo &dev, const void *W, const void *x, void *
     return launch_tma<P, NV, R, false>(a, p, stream);
 }
 
+// The launch policy of a dense matvec: format P at NV vectors on rows of
+// `cols` columns.  Calls f(policy, rows-per-lane) with the chosen policy type
+// and R as an integral_constant; the launch and the test-only plan query
+// (hq_debug_plan) both go through here, so they cannot disagree.
+template <class P, int NV, class F>
+hq_status with_dense_policy(long long cols, F &&f) {
+    constexpr int R = rows_per_lane<P>(NV);
+    using RT = std::integral_constant<int, R>;
+    if constexpr (std::is_same<P, PolQ8_0>::value && NV == 1) {
+        if (cols <= kShortRowCols) return f(PolQ8_0Short{}, RT{});
+        return f(P{}, RT{});
+    } else if constexpr (std::is_same<P, PolQ8_0>::value && NV == 2) {
+        return f(PolQ8_0Two{}, RT{});
+    } else if constexpr (std::is_same<P, PolQ8_0>::value) {
+        // Q8_0 at three or more vectors: row-split stages, one x tile per CTA
+        // (8B-shaped token at n_vec 3 / 4 / 6 / 8: 2674 / 2255 / 1654 / 1310 ->
+        // 3240 / 2730 / 1720 / 1328 GB/s; at n_vec 2 no gain).  Q4_0 keeps one
+        // owner per stage: with its 128-row split stages it measured 1866 / 1605 /
+        // 1007 -> 1794 / 1586 / 926 GB/s at n_vec 3 / 4 / 8.
+        return f(PolRowSplit<P>{}, RT{});
+    } else {
+        return f(P{}, RT{});
+    }
+}
+
 template <class P, int NV>
 hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y, const int32_t *mult,
                    const int32_t *shift, long long rows, long long cols, const LoraArgs *lora,
                    cudaStream_t stream) {
-    constexpr int R = rows_per_lane<P>(NV);
-    if constexpr (std::is_same<P, PolQ8_0>::value && NV == 1)
-        if (cols <= kShortRowCols)
-            return dense_nv_r<PolQ8_0Short, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
-    // Q8_0 at three or more vectors: row-split stages, one x tile per CTA
-    // (8B-shaped token at n_vec 3 / 4 / 6 / 8: 2674 / 2255 / 1654 / 1310 ->
-    // 3240 / 2730 / 1720 / 1328 GB/s; at n_vec 2 no gain).  Q4_0 keeps one
-    // owner per stage: with its 128-row split stages it measured 1866 / 1605 /
-    // 1007 -> 1794 / 1586 / 926 GB/s at n_vec 3 / 4 / 8.
-    if constexpr (NV == 2 && std::is_same<P, PolQ8_0>::value)
-        return dense_nv_r<PolQ8_0Two, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
-    if constexpr (NV >= 3 && std::is_same<P, PolQ8_0>::value)
-        return dense_nv_r<PolRowSplit<P>, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
-    return dense_nv_r<P, NV, R>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
+    return with_dense_policy<P, NV>(cols, [&](auto pol, auto rt) {
+        return dense_nv_r<decltype(pol), NV, decltype(rt)::value>(dev, W, x, y, mult, shift, rows, cols, lora,
+                                                                   stream);
+    });
+}
+
+// Policy identifiers reported by the plan query.
+template <class Pol>
+constexpr int policy_id() {
+    return std::is_same<Pol, PolQ8_0Short>::value ? 1
+         : std::is_same<Pol, PolQ8_0Two>::value ? 2
+         : Pol::kRowSplit ? 3 : 0;
+}
+
+// Test-only: the geometry make_plan gives one dense launch, for a device
+// described by `dev` (only num_sms and max_smem_optin are read) and a kernel
+// of `regs` registers per thread.
+template <class P, int NV>
+hq_status dense_plan(const DeviceInfo &dev, long long rows, long long cols, int regs, int64_t *out) {
+    return with_dense_policy<P, NV>(cols, [&](auto pol, auto rt) {
+        using Pol = decltype(pol);
+        constexpr int R = decltype(rt)::value;
+        using L = Layout<Pol, NV, R, false>;
+        const long long tiles = (rows + L::TR - 1) / L::TR;
+        const Plan p = make_plan<Pol, NV, R, false>(dev, tiles, (int)(cols / Pol::kChunkCols), regs);
+        out[0] = policy_id<Pol>();
+        out[1] = cons_warps<Pol, NV, R>();
+        out[2] = L::TR;
+        out[3] = p.grid;
+        out[4] = p.ksplit;
+        out[5] = p.stages;
+        out[6] = (int64_t)p.smem;
+        out[7] = ctas_per_sm<Pol, NV, R>();
+        out[8] = p.slots;
+        out[9] = tiles;
+        return HQ_OK;
+    });
+}
+
+template <class P>
+hq_status plan_dispatch(const DeviceInfo &dev, long long rows, long long cols, int n_vec, int regs, int64_t *out) {
+    switch (n_vec) {
+        case 1: return dense_plan<P, 1>(dev, rows, cols, regs, out);
+        case 2: return dense_plan<P, 2>(dev, rows, cols, regs, out);
+        case 3: return dense_plan<P, 3>(dev, rows, cols, regs, out);
+        case 4: return dense_plan<P, 4>(dev, rows, cols, regs, out);
+        case 5: return dense_plan<P, 5>(dev, rows, cols, regs, out);
+        case 6: return dense_plan<P, 6>(dev, rows, cols, regs, out);
+        case 7: return dense_plan<P, 7>(dev, rows, cols, regs, out);
+        case 8: return dense_plan<P, 8>(dev, rows, cols, regs, out);
+        default: return set_error(HQ_ERR_NVEC, "n_vec %d not in [1,8]", n_vec);
+    }
 }
 
 template <class P>
@@ -1691,7 +1754,26 @@ hq_status HQ_PART_NAME(launch_matvec_float)(const void *W, const float *x, float
 }
 #endif
 
+#if !defined(HQ_PART) || HQ_PART == 0 || HQ_PART == 1
+hq_status HQ_PART_NAME(debug_plan_float)(int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin,
+                                         int regs, int64_t *out) {
+    using P = std::conditional<HQ_PART == 1, PolQ4_0, PolQ8_0>::type;
+    DeviceInfo dev;
+    dev.num_sms = num_sms;
+    dev.max_smem_optin = smem_optin;
+    return plan_dispatch<P>(dev, rows, cols, n_vec, regs, out);
+}
+#endif
+
 #if HQ_PART == 2
+hq_status debug_plan_i8(int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin, int regs,
+                        int64_t *out) {
+    DeviceInfo dev;
+    dev.num_sms = num_sms;
+    dev.max_smem_optin = smem_optin;
+    return plan_dispatch<PolI8>(dev, rows, cols, n_vec, regs, out);
+}
+
 hq_status launch_matvec_i8(const int8_t *W, const int8_t *x, const int32_t *mult,
                            const int32_t *shift, int8_t *y, int64_t rows, int64_t cols, int n_vec,
                            cudaStream_t stream) {
