@@ -4,7 +4,7 @@ launch would get, touching no GPU.
 
 Two kinds of checks:
   * pins: the geometry of the bench's launches as ncu recorded them on a GB300
-    (grid x block and dynamic shared memory in the committed profiles), for a
+    (grid x block and dynamic shared memory in the committed ncu summaries), for a
     device of 152 SMs with 227 KB (232,448 B) of opt-in shared memory per CTA
     and the kernels' register counts from `ptxas -v` of the sm_103a build;
   * invariants over a sweep of shapes, vector counts and formats: every stage
@@ -34,9 +34,9 @@ def plan(hq, fmt, n_vec, rows, cols, regs):
     return hq.hq_debug_plan(fmt, n_vec, rows, cols, GB300["num_sms"], GB300["smem_optin"], regs)
 
 
-# (fmt, n_vec, rows, cols, regs) -> (grid, threads per CTA, K split, dynamic smem bytes or None)
-# from profiles/matvec_q8_0_8b_decode_token_launches.md, matvec_q4_0_8b_decode_token_launches.md,
-# matvec_q8_0_qwen3_0.6b_decode_token_launches.md and the full captures.
+# (fmt, n_vec, rows, cols, regs) -> (grid, threads per CTA, K split, dynamic smem bytes or None),
+# as ncu recorded them for the 8B-shaped Q8_0 and Q4_0 tokens, the Qwen3-0.6B-shaped token and the
+# full captures of single matrices (the ncu summaries committed beside the benchmark).
 PINS = [
     ((8, 1, 28672, 4096, 78), (448, 96, 1, 58880)),      # Q8_0 gate|up: 2 tiles per CTA, 6-stage ring
     ((8, 1, 4096, 14336, 78), (512, 96, 4, None)),       # down: clusters of 4
