@@ -662,7 +662,7 @@ def main():
     model, fmt, ops = workload_ops(args.workload, args.n_vec, args.shape, args.format)
     kind = WORKLOADS[args.workload][0] if not args.shape else "dense"
     config = {"workload": describe_workload(args, model, fmt, ops, kind),
-              "model_shape": model, "format": fmt, "n_vec": args.n_vec, "launches_per_step": len(ops),
+              "shape_set": model, "format": fmt, "n_vec": args.n_vec, "launches_per_step": len(ops),
               "l2": (f"inputs larger than L2: every launch reads its own weights, "
                      f"{sum(op.weight_bytes() for op in ops) / 1e9:.2f} GB per step"),
               "seed": synthetic.SEED_BASE + 2}
