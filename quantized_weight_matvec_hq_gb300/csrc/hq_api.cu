@@ -33,6 +33,9 @@ thread_local char t_error[512] = "";
 std::mutex g_mutex;
 constexpr int kMaxDevices = 64;
 DeviceInfo g_devices[kMaxDevices];
+// g_ready[d] == d + 1 once g_devices[d] is complete: written (release) after
+// the record under g_mutex, read (acquire) before the record without it.
+std::atomic<int> g_ready[kMaxDevices];
 void *g_encoder = nullptr;
 bool g_encoder_tried = false;
 
@@ -54,9 +57,9 @@ hq_status device_info(DeviceInfo **out) {
     if (e != cudaSuccess) return set_error(HQ_ERR_UNSUPPORTED, "no CUDA device: %s", cudaGetErrorString(e));
     if (dev < 0 || dev >= kMaxDevices) return set_error(HQ_ERR_UNSUPPORTED, "device index %d too large", dev);
     DeviceInfo &d = g_devices[dev];
-    if (d.device == dev) { *out = &d; return HQ_OK; }
+    if (g_ready[dev].load(std::memory_order_acquire) == dev + 1) { *out = &d; return HQ_OK; }
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (d.device != dev) {
+    if (g_ready[dev].load(std::memory_order_relaxed) != dev + 1) {
         DeviceInfo n;
         n.device = dev;
         if (cudaDeviceGetAttribute(&n.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
@@ -74,6 +77,7 @@ hq_status device_info(DeviceInfo **out) {
         if (e != cudaSuccess) return set_error(HQ_ERR_UNSUPPORTED, "adapter scratch: %s", cudaGetErrorString(e));
         n.lora_scratch = static_cast<float *>(p);
         d = n;
+        g_ready[dev].store(dev + 1, std::memory_order_release);
     }
     *out = &d;
     return HQ_OK;

@@ -42,6 +42,7 @@
 #include <stdlib.h>
 
 #include <algorithm>
+#include <mutex>
 #include <type_traits>
 
 #include "hq_device.cuh"
@@ -1445,6 +1446,8 @@ long long max_active_clusters(const DeviceInfo &dev, int G, size_t smem) {
     struct Entry { int device, G; size_t smem; long long n; };
     static Entry cache[32];
     static int used = 0;
+    static std::mutex mu;                        // launches may come from several host threads
+    std::lock_guard<std::mutex> lock(mu);
     for (int i = 0; i < used; ++i)
         if (cache[i].device == dev.device && cache[i].G == G && cache[i].smem == smem) return cache[i].n;
     auto kern = matvec_tma_kernel<P, NV, R, MOE>;
