@@ -772,9 +772,10 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 template <class P, int NV, int R>
 constexpr int ctas_per_sm() {
     if constexpr (P::kRowSplit) return NV <= 4 ? 5 : 4;
-    // Q4_0 at 3-6 vectors: its 96-116 registers leave room for a third CTA
-    // (8B-shaped token n_vec 3 / 4: 1865 / 1606 -> 1939 / 1651 GB/s)
-    if constexpr (std::is_same<P, PolQ4_0>::value) if (NV >= 3 && NV <= 6) return 3;
+    // Q4_0 at 2-6 vectors: its 96-116 registers leave room for a third CTA
+    // (8B-shaped token n_vec 3 / 4: 1865 / 1606 -> 1939 / 1651 GB/s; n_vec 2,
+    // with a ring of one stage per warp: 2520 -> 2733 GB/s)
+    if constexpr (std::is_same<P, PolQ4_0>::value) if (NV >= 2 && NV <= 6) return 3;
     return cons_warps<P, NV, R>() >= 8 ? 2
          : cons_warps<P, NV, R>() >= 4 ? ((NV * R <= 2) ? 3 : 2)
                                         : ((NV * R <= 2) ? 5 : 3);
@@ -1373,6 +1374,7 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     // Q8_0 kernel at one vector does not (8B token 5186 -> 4607 GB/s), nor the
     // MoE kernel at four vectors (2696 -> 2579 GB/s).
     constexpr int kSpw = (((std::is_same<P, PolQ4_0>::value || std::is_same<P, PolQ8_0Moe>::value) && NV == 1) ||
+                          (std::is_same<P, PolQ4_0>::value && NV == 2) ||
                           (std::is_same<P, PolQ8_0Two>::value && NV == 2)) ? 1 : 2;
     p.stages = kSpw * SQ;
     while (L::total(p.stages + SQ, 1) * want <= budget && p.stages < 4 * SQ) p.stages += SQ;
