@@ -73,6 +73,38 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     return LIB
 
 
+def kernel_resources(out_dir: str) -> dict:
+    """Compile the kernel translation units (not linked, not installed) into
+    `out_dir` with `ptxas -v` and return {mangled kernel name: (registers per
+    thread, spill store bytes, spill load bytes)}."""
+    import re
+    os.makedirs(out_dir, exist_ok=True)
+    nvcc = _nvcc()
+    jobs = [[nvcc, *ARCH, *NVCC_FLAGS, "-Xptxas", "-v", *defs, "-c", os.path.join(CSRC, src),
+             "-o", os.path.join(out_dir, obj)]
+            for src, defs, obj in SOURCES if src == "hq_kernels.cu"]
+    with cf.ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        results = list(ex.map(lambda c: subprocess.run(c, capture_output=True, text=True), jobs))
+    res, name, spill = {}, None, (0, 0)
+    for r in results:
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed: " + r.stderr[-2000:])
+        for ln in r.stderr.splitlines():
+            m = re.search(r"Compiling entry function '([^']+)'", ln)
+            if m:
+                name = m.group(1)
+                continue
+            m = re.search(r"(\d+) bytes spill stores, (\d+) bytes spill loads", ln)
+            if m:
+                spill = (int(m.group(1)), int(m.group(2)))
+                continue
+            m = re.search(r"Used (\d+) registers", ln)
+            if m and name:
+                res[name] = (int(m.group(1)), *spill)
+                name, spill = None, (0, 0)
+    return res
+
+
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
                 extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else None))
