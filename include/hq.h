@@ -85,8 +85,11 @@ const char *hq_last_error(void);
  *   x  : fp32 [n_vec][cols], 16-byte aligned.
  *   y  : fp32 [n_vec][rows], overwritten (not accumulated).
  * Accumulation is fp32; |y - y_exact| <= 1e-3 * sum_j |w_deq[i][j] * x[v][j]| + 1e-5
- * for finite x with |x| < 2^64 (at n_vec <= 2 the kernel rescales x by 2^64,
- * exactly, and larger |x| would overflow to inf).
+ * for finite x with |x| < 2^100 (beyond that a block's partial sum may
+ * overflow).  Every quant is decoded to its signed value exactly before it
+ * multiplies x, so the rounding is relative to the products |w x| themselves:
+ * the bound holds at every n_vec for sparse or outlier-dominated blocks and
+ * for x of any sign pattern or mean.
  * Source: "One Native Stack ...", section "The Unified Quant Core" (Q8_0,
  * 34 B/32) and the Lemma of section "The Central Efficiency Thesis".
  */
@@ -96,7 +99,7 @@ hq_status hq_matvec_q8_0(const void *W, const float *x, float *y,
 /*
  * hq_matvec_q4_0 -- as hq_matvec_q8_0 for Q4_0 blocks (rows x cols/32 x 18 B):
  * w = d * (n - 8), nibble order as in the conventions above; the same
- * accuracy and the same |x| < 2^64 precondition.
+ * accuracy and the same |x| < 2^100 precondition.
  * Source: "One Native Stack ...", section "The Unified Quant Core" (Q4_0, 18 B/32).
  */
 hq_status hq_matvec_q4_0(const void *W, const float *x, float *y,
@@ -181,7 +184,7 @@ hq_status hq_matvec_i8_requant(const int8_t *W, const int8_t *x,
  *                share x[t], as for gate/up), or [n_vec][n_active][cols] when
  *                x_per_slot == 1 (one input per slot, as for down).
  *   y          : fp32 [n_vec][n_active][rows]; y[t][k] = W_bank[ids[t][k]] . x(t,k).
- * Accuracy and the |x| < 2^64 precondition as for hq_matvec_q8_0.
+ * Accuracy and the |x| < 2^100 precondition as for hq_matvec_q8_0.
  * Slots that pick the same expert are grouped so that each chosen expert's
  * bytes are streamed once per call.  No router weighting is applied (the
  * _combine variant below applies it).  An id

@@ -72,38 +72,6 @@ __device__ __forceinline__ float byte_as_float(uint32_t word, int byte) {
     return __uint_as_float(prmt(word, kMagic, 0x7540u | (uint32_t)byte));
 }
 
-// Scale a stage's fp32 x tile ([NV][256]) in place by 2^64 (exact for
-// |x| < 2^64) and return, per lane, the sum of the 2^64-scaled x of 32-column
-// block lane/4 times XS_MUL (every lane of a group of four holds it).  Used by
-// the decodes that read quants as fp32 subnormals: the products
-// quant * 2^-149 * x * 2^64 are then normal numbers, rounded like any fp32
-// product.  With HI_16 the second half of every block (columns 16..31) is
-// scaled by 2^60 instead, so that a nibble read 4 bits higher in its byte
-// gives a product on the same scale as the low nibble's.
-template <int NV, bool HI_16 = false>
-__device__ __forceinline__ void scale_x_tile(uint8_t *xt8, int lane, float (&xs)[NV], float xs_mul = 1.0f) {
-    float4 *xt = reinterpret_cast<float4 *>(xt8);
-    const bool hi = HI_16 && (lane & 2);              // this lane's 8 columns are 16..31 of their block
-    const float ks = hi ? 0x1p60f : 0x1p64f;
-    const float2 k64 = make_float2(ks, ks), z = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        float4 a = xt[v * 64 + 2 * lane], b = xt[v * 64 + 2 * lane + 1];
-        const float2 a0 = ffma2(make_float2(a.x, a.y), k64, z), a1 = ffma2(make_float2(a.z, a.w), k64, z);
-        const float2 b0 = ffma2(make_float2(b.x, b.y), k64, z), b1 = ffma2(make_float2(b.z, b.w), k64, z);
-        a = make_float4(a0.x, a0.y, a1.x, a1.y);
-        b = make_float4(b0.x, b0.y, b1.x, b1.y);
-        xt[v * 64 + 2 * lane] = a;
-        xt[v * 64 + 2 * lane + 1] = b;
-        float t = ((a.x + a.y) + (a.z + a.w)) + ((b.x + b.y) + (b.z + b.w));
-        if (hi) t *= 16.0f;                           // back to the 2^64 scale (exact)
-        t += __shfl_xor_sync(0xffffffffu, t, 1);
-        t += __shfl_xor_sync(0xffffffffu, t, 2);
-        xs[v] = t * xs_mul;
-    }
-    __syncwarp();
-}
-
 struct PolQ8_0 {
     static constexpr int kBlockBytes = 34;
     static constexpr int kChunkCols = 256;          // 8 blocks
@@ -115,111 +83,20 @@ struct PolQ8_0 {
     static constexpr int kConsWarps = 2;            // memory-bound: few warps per CTA, more CTAs
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
-    static constexpr bool kMayScaleX = true;        // prepare() may rescale the stage's x tile
     static constexpr bool kRowSplit = false;        // see PolRowSplit
-    // one vector: quants read as subnormals (no bias add per pair); more
-    // (measured at two: 3688 against 3537 GB/s): through the exponent of 2^23,
-    // x as stored
-    template <int NV> static constexpr bool scaled_x() { return NV == 1; }
     using Acc = float2;
     using Red = float;
 
-    template <int NV>
-    __device__ __forceinline__ static void prepare(uint8_t *xt8, int lane, float (&xs)[NV]) {
-        if constexpr (scaled_x<NV>()) scale_x_tile<NV>(xt8, lane, xs);
-    }
-
+    // Per lane: R rows x blocks [B0, B0+NB) of one chunk of the stage.  The
+    // quant byte q XOR 0x80 (= q + 128, in [1, 255]) is placed by one prmt in
+    // the low mantissa bits of 2^23, and a packed add of -(2^23 + 128) leaves
+    // q exactly: every product q * x is then formed exactly inside the FMA and
+    // the running sums only ever hold partial sums of q * x, so the rounding is
+    // bounded by the sizes of |q * x|, whatever the signs and magnitudes of x.
     template <int NV, int R, int B0, int NB>
     __device__ __forceinline__ static void consume(const uint8_t *__restrict__ wt,
                                                    const uint8_t *__restrict__ xt8, int lane,
-                                                   Acc (&acc)[R][NV], const float (&xs)[NV]) {
-        if constexpr (scaled_x<NV>()) consume_subnormal<NV, R, B0, NB>(wt, xt8, lane, acc, xs);
-        else consume_magic<NV, R, B0, NB>(wt, xt8, lane, acc);
-    }
-
-    // Quant q (int8) plus 128 is a byte in [1, 255]; prmt moves it alone into a
-    // zeroed word, read as the fp32 subnormal (q + 128) * 2^-149 exactly.  With
-    // x scaled by 2^64 the products are normal; the offset 128 is removed once
-    // per block as -128 * d * (the block's x sum).
-    template <int NV, int R, int B0, int NB>
-    __device__ __forceinline__ static void consume_subnormal(const uint8_t *__restrict__ wt,
-                                                             const uint8_t *__restrict__ xt8, int lane,
-                                                             Acc (&acc)[R][NV], const float (&xs)[NV]) {
-        const float *xt = reinterpret_cast<const float *>(xt8);
-        constexpr int NCH = (R * NV >= 4) ? 1 : 2;
-        const uint4 *rowp[R];
-        uint4 c0[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            rowp[r] = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes);
-            c0[r] = rowp[r][2 * B0];
-        }
-#pragma unroll
-        for (int b = B0; b < B0 + NB; ++b) {
-            uint32_t win[R][12];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const uint4 c1 = rowp[r][2 * b + 1], c2 = rowp[r][2 * b + 2];
-                win[r][0] = c0[r].x; win[r][1] = c0[r].y; win[r][2] = c0[r].z; win[r][3] = c0[r].w;
-                win[r][4] = c1.x; win[r][5] = c1.y; win[r][6] = c1.z; win[r][7] = c1.w;
-                win[r][8] = c2.x; win[r][9] = c2.y; win[r][10] = c2.z; win[r][11] = c2.w;
-                c0[r] = c2;
-            }
-            float2 s[R][NV][NCH];
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int v = 0; v < NV; ++v)
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) s[r][v][c] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                float4 xv[NV];
-#pragma unroll
-                for (int v = 0; v < NV; ++v)
-                    xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * b + 4 * g);
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    float f[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int o = 2 * b + 2 + 4 * g + i;      // window byte of quant 4g+i
-                        f[i] = __uint_as_float(prmt(win[r][o >> 2] ^ 0x80808080u, 0u, 0x4440u | (uint32_t)(o & 3)));
-                    }
-#pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        float2 &sv = s[r][v][g % NCH];
-                        sv = ffma2(make_float2(f[0], f[1]), make_float2(xv[v].x, xv[v].y), sv);
-                        sv = ffma2(make_float2(f[2], f[3]), make_float2(xv[v].z, xv[v].w), sv);
-                    }
-                }
-            }
-            float xb[NV];                                       // the block's scaled x sum
-#pragma unroll
-            for (int v = 0; v < NV; ++v) xb[v] = __shfl_sync(0xffffffffu, xs[v], 4 * b);
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const uint32_t sw = win[r][b >> 1];               // fp16 d at window byte 2b
-                const unsigned short hb = (b & 1) ? (unsigned short)(sw >> 16) : (unsigned short)(sw & 0xffffu);
-                const float d = __half2float(__ushort_as_half(hb));
-                const float2 dd = make_float2(d * 0x1p85f, d * 0x1p85f);
-                const float dbias = d * -0x1p-57f;                 // -128 * d * 2^-64
-#pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    float2 t = s[r][v][0];
-                    if (NCH == 2) t = fadd2(t, s[r][v][NCH - 1]);
-                    acc[r][v] = ffma2(dd, t, acc[r][v]);
-                    acc[r][v].x = fmaf(dbias, xb[v], acc[r][v].x);
-                }
-            }
-        }
-    }
-
-    // per lane: R rows x blocks [B0, B0+NB) of one chunk of the stage
-    template <int NV, int R, int B0, int NB>
-    __device__ __forceinline__ static void consume_magic(const uint8_t *__restrict__ wt,
-                                                         const uint8_t *__restrict__ xt8, int lane,
-                                                         Acc (&acc)[R][NV]) {
+                                                   Acc (&acc)[R][NV]) {
         const float *xt = reinterpret_cast<const float *>(xt8);
         constexpr int NCH = (R * NV >= 4) ? 1 : 2;               // independent FMA chains
         const float2 kOff = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
@@ -313,12 +190,13 @@ struct PolQ8_0Two : PolQ8_0 {
     static constexpr int kConsWarpsFewAcc = 3;
 };
 
-// Q4_0 nibble decode for three or more vectors, one and-or per element: a
-// nibble at bit p in {0, 4, 8, 12}, masked in place and ORed into the
-// exponent of 2^23, is the fp32 value 2^23 + q * 2^p (exact: the mantissa has
-// 23 bits); adding -(2^23 + 8 * 2^p) leaves (q - 8) * 2^p exactly.  The
-// exponent bits live in a register the compiler cannot see through, so the
-// mask-and-OR stays one lop3 with the mask as its immediate.
+// Q4_0 nibble decode, one and-or per element: a nibble at bit p in {0, 4, 8,
+// 12}, masked in place and ORed into the exponent of 2^23, is the fp32 value
+// 2^23 + n * 2^p (exact: the mantissa has 23 bits); adding -(2^23 + 8 * 2^p)
+// leaves (n - 8) * 2^p exactly, so the running sums only ever hold partial
+// sums of signed weight times x.  The exponent bits live in a register the
+// compiler cannot see through, so the mask-and-OR stays one lop3 with the
+// mask as its immediate.
 __device__ __forceinline__ uint32_t opaque_magic() {
     uint32_t m;
     asm volatile("mov.b32 %0, 0x4B000000;" : "=r"(m));
@@ -331,18 +209,11 @@ __device__ __forceinline__ float nib(uint32_t w, uint32_t magic) {
     return __uint_as_float(r);
 }
 
-// Q4_0 nibble decode for one or two vectors, one and per element.  A nibble at bit position
-// p in {0, 4, 8, 12} of a word, masked in place and read as fp32, is the
-// subnormal q * 2^(p-149) -- exactly.  x is first scaled in shared memory by
-// 2^64 in the first half of every block and by 2^60 in the second (exact for
-// |x| < 2^64), so a low nibble (element t, bits p) and a high nibble (element
-// t + 16, bits p + 4) give products on the same scale, q * x * 2^(p-85): every
-// one a normal number, rounded like any fp32 product, summed into one
-// accumulator.  Two adjacent quant bytes always lie in one 16-bit half of a
-// word (the upper half is shifted down), so a pair of elements sits at bits
-// (0, 8) or (4, 12): the accumulator's two lanes carry the scales 2^-85 and
-// 2^-77, joined by exact powers of two once per block, where the offset 8 of
-// every nibble is applied through the block's x sum.
+// Two adjacent quant bytes always lie in one 16-bit half of a word (the
+// upper half is shifted down once), so every pair of low nibbles sits at bits
+// (0, 8) and every pair of high nibbles at bits (4, 12); the two positions of
+// a pair are summed apart and their 2^p factors are removed once per block by
+// exact powers of two.
 struct PolQ4_0 {
     static constexpr int kBlockBytes = 18;
     static constexpr int kChunkCols = 256;          // 8 blocks
@@ -354,113 +225,15 @@ struct PolQ4_0 {
     static constexpr int kConsWarps = 4;            // nibble decode is ALU-heavy: more warps hide its latency
     static constexpr int kConsWarpsFewAcc = 4;      // n_vec 1 (two rows per lane; see make_plan's ring)
     static constexpr bool kComputeBound = true;     // decode, not HBM, sets the pace
-    static constexpr bool kMayScaleX = true;        // prepare() may rescale the stage's x tile
     static constexpr bool kRowSplit = false;
-    // the subnormal decode (one and per nibble, x scaled by 2^64) pays off at
-    // one or two vectors; with more, the per-vector block sums cost more than
-    // the bias adds the exponent-OR decode needs
-    template <int NV> static constexpr bool scaled_x() { return NV <= 2; }
-    using Acc = float2;                             // (elements at nibble bits 0/4, at bits 8/12) x 2^-8
+    using Acc = float2;
     using Red = float;
 
-    template <int NV>
-    __device__ __forceinline__ static void prepare(uint8_t *xt8, int lane, float (&xs)[NV]) {
-        if constexpr (scaled_x<NV>()) scale_x_tile<NV, true>(xt8, lane, xs, -0x1p-146f);
-    }
-
+    // per lane: R rows x blocks [B0, B0+NB) of one chunk of the stage
     template <int NV, int R, int B0, int NB>
     __device__ __forceinline__ static void consume(const uint8_t *__restrict__ wt,
                                                    const uint8_t *__restrict__ xt8, int lane,
-                                                   Acc (&acc)[R][NV], const float (&xs)[NV]) {
-        if constexpr (scaled_x<NV>()) consume_subnormal<NV, R, B0, NB>(wt, xt8, lane, acc, xs);
-        else consume_magic<NV, R, B0, NB>(wt, xt8, lane, acc);
-    }
-
-    // x scaled by 2^64 / 2^60 (prepare), nibbles read as subnormals
-    template <int NV, int R, int B0, int NB>
-    __device__ __forceinline__ static void consume_subnormal(const uint8_t *__restrict__ wt,
-                                                             const uint8_t *__restrict__ xt8, int lane,
-                                                             Acc (&acc)[R][NV], const float (&xs)[NV]) {
-        const float *xt = reinterpret_cast<const float *>(xt8);
-        constexpr int NCH = (R * NV >= 4) ? 1 : 2;               // independent FMA chains
-        const float2 kScale = make_float2(0x1p85f, 0x1p77f);    // bits 0/4 carry 2^-85, bits 8/12 2^-77
-        const uint4 *rowp[R];
-        uint4 c0[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            rowp[r] = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes);
-            c0[r] = rowp[r][B0];
-        }
-#pragma unroll
-        for (int b = B0; b < B0 + NB; ++b) {
-            // window = 16-byte units b, b+1: block b's scale is window bytes 2b, 2b+1
-            // and its quant byte t is window byte 2b + 2 + t (low nibble: element t,
-            // high nibble: element t + 16)
-            uint32_t win[R][8], sw[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const uint4 c1 = rowp[r][b + 1];
-                win[r][0] = c0[r].x; win[r][1] = c0[r].y; win[r][2] = c0[r].z; win[r][3] = c0[r].w;
-                win[r][4] = c1.x; win[r][5] = c1.y; win[r][6] = c1.z; win[r][7] = c1.w;
-                sw[r] = win[r][b >> 1];
-                c0[r] = c1;
-            }
-            float2 s[R][NV][NCH];
-#pragma unroll
-            for (int r = 0; r < R; ++r)
-#pragma unroll
-                for (int v = 0; v < NV; ++v)
-#pragma unroll
-                    for (int c = 0; c < NCH; ++c) s[r][v][c] = make_float2(0.f, 0.f);
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                float4 xv[NV];
-#pragma unroll
-                for (int v = 0; v < NV; ++v)
-                    xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * b + 4 * g);
-                const bool high = g >= 4;                   // elements 16..31: high nibbles
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const int t = (4 * g + 2 * h) & 15;     // first quant byte of the pair
-                        const int o = 2 * b + 2 + t;            // its window byte (even)
-                        const uint32_t w = (o & 2) ? (win[r][o >> 2] >> 16) : win[r][o >> 2];
-                        const float2 q = high ? make_float2(__uint_as_float(w & 0xF0u), __uint_as_float(w & 0xF000u))
-                                              : make_float2(__uint_as_float(w & 0xFu), __uint_as_float(w & 0xF00u));
-#pragma unroll
-                        for (int v = 0; v < NV; ++v) {
-                            const float2 xp = h ? make_float2(xv[v].z, xv[v].w) : make_float2(xv[v].x, xv[v].y);
-                            float2 &sv = s[r][v][h % NCH];
-                            sv = ffma2(q, xp, sv);
-                        }
-                    }
-                }
-            }
-            float xb[NV];                                       // -2^-146 x the block's 2^64-scaled x sum
-#pragma unroll
-            for (int v = 0; v < NV; ++v) xb[v] = __shfl_sync(0xffffffffu, xs[v], 4 * b);
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const unsigned short hb = (b & 1) ? (unsigned short)(sw[r] >> 16) : (unsigned short)(sw[r] & 0xffffu);
-                const float d = __half2float(__ushort_as_half(hb));
-                const float2 dd = __fmul2_rn(make_float2(d, d), kScale);
-#pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    float2 t = s[r][v][0];
-                    if (NCH == 2) t = fadd2(t, s[r][v][NCH - 1]);
-                    t.x += xb[v];                                // d * 2^85 * xb = -8 * d * (the block's x sum)
-                    acc[r][v] = ffma2(dd, t, acc[r][v]);
-                }
-            }
-        }
-    }
-
-    // x as stored, nibbles through the exponent of 2^23 and a bias add
-    template <int NV, int R, int B0, int NB>
-    __device__ __forceinline__ static void consume_magic(const uint8_t *__restrict__ wt,
-                                                         const uint8_t *__restrict__ xt8, int lane,
-                                                         Acc (&acc)[R][NV]) {
+                                                   Acc (&acc)[R][NV]) {
         const float *xt = reinterpret_cast<const float *>(xt8);
         const float2 kBiasLo = make_float2(-8388616.0f, -8390656.0f);   // -(2^23 + 8), -(2^23 + 8 * 2^8)
         const float2 kBiasHi = make_float2(-8388736.0f, -8421376.0f);   // -(2^23 + 8 * 2^4), -(2^23 + 8 * 2^12)
@@ -539,18 +312,14 @@ struct PolI8 {
     static constexpr int kConsWarps = 2;
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
-    static constexpr bool kMayScaleX = false;
     static constexpr bool kRowSplit = false;
     using Acc = int;
     using Red = int;
 
-    template <int NV>
-    __device__ __forceinline__ static void prepare(uint8_t *, int, float (&)[NV]) {}
-
     template <int NV, int R, int U0, int NU>
     __device__ __forceinline__ static void consume(const uint8_t *__restrict__ wt,
                                                    const uint8_t *__restrict__ xt, int lane,
-                                                   Acc (&acc)[R][NV], const float (&)[NV]) {
+                                                   Acc (&acc)[R][NV]) {
 #pragma unroll
         for (int u = U0; u < U0 + NU; ++u) {
             int4 xu[NV];
@@ -733,14 +502,14 @@ __device__ __forceinline__ void store_swiglu_tile(const KArgs &a, const MoeTable
 // (which would cost registers and occupancy, not latency).
 template <class P, int NV, int R>
 __device__ __forceinline__ void consume_chunk(const uint8_t *wt, const uint8_t *xt, int lane,
-                                              typename P::Acc (&acc)[R][NV], const float (&xs)[NV]) {
-    P::template consume<NV, R, 0, 2>(wt, xt, lane, acc, xs);
+                                              typename P::Acc (&acc)[R][NV]) {
+    P::template consume<NV, R, 0, 2>(wt, xt, lane, acc);
     asm volatile("" ::: "memory");
-    P::template consume<NV, R, 2, 2>(wt, xt, lane, acc, xs);
+    P::template consume<NV, R, 2, 2>(wt, xt, lane, acc);
     asm volatile("" ::: "memory");
-    P::template consume<NV, R, 4, 2>(wt, xt, lane, acc, xs);
+    P::template consume<NV, R, 4, 2>(wt, xt, lane, acc);
     asm volatile("" ::: "memory");
-    P::template consume<NV, R, 6, 2>(wt, xt, lane, acc, xs);
+    P::template consume<NV, R, 6, 2>(wt, xt, lane, acc);
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -809,7 +578,6 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
     const int nthreads = blockDim.x;
     constexpr int CW = cons_warps<P, NV, R>();      // S % CW == 0 unless rows are split (see make_plan)
     constexpr bool RS = P::kRowSplit;
-    if constexpr (RS) static_assert(!P::template scaled_x<NV>(), "row-split stages need a decode that leaves x as it is");
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
@@ -974,9 +742,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 mbar_wait(smem_u32(&full[s]), (n / S) & 1, abort_flag, a.fault);
                 uint8_t *st = smem + (size_t)s * ST;
                 if constexpr (!MOE) {
-                    float xs[NV];
-                    P::template prepare<NV>(st + WT, lane, xs);
-                    consume_chunk<P, NV, R>(st + (RS ? (size_t)warp * 32 * R * P::kChunkBytes : 0), st + WT, lane, acc, xs);
+                    consume_chunk<P, NV, R>(st + (RS ? (size_t)warp * 32 * R * P::kChunkBytes : 0), st + WT, lane, acc);
                 } else {
                     // only the group's m vectors are multiplied
                     switch (m) {
@@ -986,9 +752,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
             Acc acc_m[R][M_];                                                        \
             _Pragma("unroll") for (int r = 0; r < R; ++r)                            \
                 _Pragma("unroll") for (int v = 0; v < M_; ++v) acc_m[r][v] = acc[r][v]; \
-            float xs_m[M_];                                                          \
-            P::template prepare<M_>(st + WT, lane, xs_m);                            \
-            consume_chunk<P, M_, R>(st, st + WT, lane, acc_m, xs_m);                 \
+            consume_chunk<P, M_, R>(st, st + WT, lane, acc_m);                       \
             _Pragma("unroll") for (int r = 0; r < R; ++r)                            \
                 _Pragma("unroll") for (int v = 0; v < M_; ++v) acc[r][v] = acc_m[r][v]; \
         }                                                                            \
@@ -999,7 +763,6 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                         default: break;
                     }
                 }
-                if constexpr (P::kMayScaleX) fence_proxy_async_shared(); // our x writes before the next copy into the stage
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
             }
@@ -1318,36 +1081,6 @@ hq_status encode_2d(CUtensorMap *m, CUtensorMapDataType dt, const void *base, ui
     return HQ_OK;
 }
 
-// Largest K split (CTAs per cluster); HQ_MAX_KSPLIT overrides it for tuning.
-int max_ksplit() {
-    static int v = -1;
-    if (v < 0) {
-        const char *e = getenv("HQ_MAX_KSPLIT");
-        v = e ? std::max(1, std::min(kMaxSplit, atoi(e))) : kMaxSplit;
-    }
-    return v;
-}
-
-// A ring no deeper than the CTA's own fills (HQ_RING_CAP=0 turns it off, for comparison).
-bool ring_cap() {
-    static int v = -1;
-    if (v < 0) {
-        const char *e = getenv("HQ_RING_CAP");
-        v = (e && atoi(e) == 0) ? 0 : 1;
-    }
-    return v == 1;
-}
-
-// Deeper rings when fewer CTAs share an SM (HQ_ADAPTIVE_RING=0 turns it off, for comparison).
-bool adaptive_ring() {
-    static int v = -1;
-    if (v < 0) {
-        const char *e = getenv("HQ_ADAPTIVE_RING");
-        v = (e && atoi(e) == 0) ? 0 : 1;
-    }
-    return v == 1;
-}
-
 // Launch geometry: ctas_per_sm<P,NV,R>() CTAs per SM, the stage ring sized to
 // share the SM's shared memory among them.  Row tiles are 32*R rows; when
 // there are too few to fill every CTA slot, K is split across a cluster of up
@@ -1386,7 +1119,7 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     const long long slots = (long long)dev.num_sms * per_sm;
     int ks = 1;
     p.slots = slots;
-    while (gsplit == 0 && ks < max_ksplit() && n_work * ks * 2 <= slots && n_chunks >= 2 * ks) ks *= 2;
+    while (gsplit == 0 && ks < kMaxSplit && n_work * ks * 2 <= slots && n_chunks >= 2 * ks) ks *= 2;
     p.ksplit = ks;
     p.gsplit = std::max(gsplit, 1);
     // gather-buffer slots: the K split's partials, or a combine's own partial sums
@@ -1411,9 +1144,8 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     int st = p.stages;
     const int st_min = P::kRowSplit ? 2 : CW;
     while (st > st_min && L::total(st, lks) * resident > budget) st -= SQ;    // room for the gather buffer
-    if (adaptive_ring())
-        while (st + SQ <= 16 && L::total(st + SQ, lks) * resident <= budget) st += SQ;
-    if (ring_cap()) {
+    while (st + SQ <= 16 && L::total(st + SQ, lks) * resident <= budget) st += SQ;
+    {
         // a CTA never has more stages than fills: the shared memory it leaves
         // lets the next kernel's CTAs become resident (and start their weight
         // copies) while this one drains

@@ -62,6 +62,20 @@ def activations(g: np.random.Generator, n_vec: int, cols: int) -> np.ndarray:
     return g.standard_normal((n_vec, cols), dtype=np.float32)
 
 
+def sparse_outlier_weights(g: np.random.Generator, rows: int, cols: int, magnitude: float = 1.0):
+    """fp32 [rows][cols] whose every 32-element block holds one element of
+    +-magnitude (random sign per row) and 31 zeros, the non-zero element at
+    the same position of the block in every row (a pruned input-channel
+    pattern).  Returns (W, outlier_cols): the column of each block's
+    non-zero element."""
+    nb = cols // 32
+    outlier_cols = np.arange(nb) * 32 + g.integers(0, 32, size=nb)
+    W = np.zeros((rows, cols), dtype=np.float32)
+    W[:, outlier_cols] = np.where(g.integers(0, 2, size=(rows, nb)) == 0, -1.0, 1.0).astype(np.float32) \
+        * np.float32(magnitude)
+    return W, outlier_cols
+
+
 def expert_ids(g: np.random.Generator, n_vec: int, n_active: int, n_experts: int) -> np.ndarray:
     """int32 [n_vec][n_active]: distinct experts per token, uniformly at random."""
     out = np.empty((n_vec, n_active), dtype=np.int32)

@@ -160,21 +160,81 @@ def test_closed_forms_on_gpu(hq, fmt):
 
 
 @pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
-@pytest.mark.parametrize("scale", [1e-30, 1e-6, 1e6, 1e15])
+@pytest.mark.parametrize("scale", [1e-40, 1e-30, 1e-6, 1e6, 1e15, 1e29])
 def test_x_magnitudes(hq, fmt, scale):
-    """x far from N(0, 1): the one- and two-vector decodes rescale x by 2^64,
-    read quants as fp32 subnormals and apply the quant offset per block; the
-    wider decode reads x as stored.  All stay within the tolerance (tiny x
-    falls back on its absolute term)."""
+    """x far from N(0, 1), up to the header's |x| < 2^100 (1e29) and down into
+    fp32 subnormals (1e-40): every decode reads x as stored, and tiny x falls
+    back on the tolerance's absolute term."""
     rows, cols = 300, 2048
     g = synthetic.rng(90)
     blocks = quant(fmt, synthetic.weights(g, rows, cols))
-    for n_vec in (1, 2, 4):
-        x = (synthetic.activations(g, n_vec, cols) * np.float32(scale)).astype(np.float32)
+    for n_vec in (1, 2, 3, 4, 8):
+        x = (synthetic.activations(g, n_vec, cols).astype(np.float64) * scale).astype(np.float32)
         y_ref, T = oracle.matvec(fmt, blocks, x, rows, cols)
         y = gpu_matvec(hq, fmt, blocks, x, rows, cols)
         assert np.all(np.isfinite(y))
         assert_within(y, y_ref, T, f"{fmt} x*{scale:g} n_vec={n_vec}")
+
+
+def _outlier_x(g, outlier_cols, n_vec, cols, kind):
+    """x for sparse outlier blocks.  "tiny": 1 everywhere except +-1e-4 at the
+    outlier columns, so sum_j |w x| is 1e-4 * |w| per block against
+    sum_j |x| of about 31; "neg": the same with alternating +-1 elsewhere;
+    "mean": N(20, 1), a large common mean."""
+    if kind == "mean":
+        return (g.standard_normal((n_vec, cols)) + 20.0).astype(np.float32)
+    x = np.ones((n_vec, cols), np.float32)
+    if kind == "neg":
+        x[:, 1::2] = -1
+    x[:, outlier_cols] = np.float32(1e-4) * np.where(
+        g.integers(0, 2, size=(n_vec, outlier_cols.size)) == 0, -1, 1).astype(np.float32)
+    return x
+
+
+# (rows, cols): many row tiles, few row tiles (K split over a cluster), the
+# plain-load kernel (cols % 256 != 0), a long row
+OUTLIER_SHAPES = [(1000, 4096), (40, 4096), (100, 992), (64, 14336)]
+
+
+@pytest.mark.parametrize("fmt", ["q8_0", "q4_0"])
+@pytest.mark.parametrize("rows,cols", OUTLIER_SHAPES)
+@pytest.mark.parametrize("kind", ["tiny", "neg", "mean"])
+def test_sparse_outlier_blocks(hq, fmt, rows, cols, kind):
+    """Blocks of one +-outlier and 31 zeros (Q8_0: q = +-127 and 0; Q4_0: the
+    outlier at n = 0, the zeros at n = 8), with x chosen so that
+    sum_j |w x| is small against sum_j |x|.  A decode that carries the quant
+    offset (q + 128, or the nibble n) through its products rounds relative to
+    128 |x| (or 8 |x|) and fails here; the bound has to hold relative to
+    |w x|, at every n_vec."""
+    g = synthetic.rng(4200 + rows + cols)
+    W, oc = synthetic.sparse_outlier_weights(g, rows, cols)
+    blocks = quant(fmt, W)
+    Wd = oracle.dequant(fmt, blocks, rows, cols)            # the zeros decode to exact zeros
+    mask = np.zeros((rows, cols), bool)
+    mask[:, oc] = True
+    assert np.all(Wd[~mask] == 0) and np.all(np.abs(Wd[mask]) > 0.99)
+    for n_vec in range(1, 9):
+        x = _outlier_x(g, oc, n_vec, cols, kind)
+        y_ref, T = oracle.matvec(fmt, blocks, x, rows, cols)
+        y = gpu_matvec(hq, fmt, blocks, x, rows, cols)
+        assert_within(y, y_ref, T, f"{fmt} {rows}x{cols} {kind} n_vec={n_vec}")
+
+
+@pytest.mark.parametrize("n_vec", [1, 2, 4, 8])
+def test_sparse_outlier_moe(hq, n_vec):
+    """The expert-indexed kernel (groups of one and of several tokens) on
+    sparse outlier experts, x = 1 except +-1e-4 at the outlier columns."""
+    n_experts, n_active, rows, cols = 16, 4, 96, 2048
+    g = synthetic.rng(4400 + n_vec)
+    W, oc = synthetic.sparse_outlier_weights(g, n_experts * rows, cols)
+    bank = quant("q8_0", W)
+    ids = synthetic.expert_ids(g, n_vec, n_active, n_experts)
+    x = _outlier_x(g, oc, n_vec, cols, "tiny")
+    y_ref, T = oracle.moe_matvec_q8_0(bank, ids, x, False, n_experts, n_active, rows, cols, n_vec)
+    y = torch.full((n_vec, n_active, rows), float("nan"), dtype=torch.float32, device="cuda")
+    hq.hq_moe_matvec_q8_0(dev(bank), dev(ids), dev(x), 0, y, n_experts, n_active, rows, cols, n_vec)
+    torch.cuda.synchronize()
+    assert_within(y.cpu().numpy(), y_ref, T, f"MoE sparse outliers n_vec={n_vec}")
 
 
 def test_deterministic_and_stream(hq):
