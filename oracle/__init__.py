@@ -43,15 +43,15 @@ def lib() -> ctypes.CDLL:
         L.hqo_half_to_float.restype = ctypes.c_float
         L.hqo_float_to_half_rne.argtypes = [ctypes.c_float]
         L.hqo_float_to_half_rne.restype = ctypes.c_uint16
-        for name in ("hqo_quantize_q8_0", "hqo_quantize_q4_0"):
+        for name in ("hqo_quantize_q8_0", "hqo_quantize_q4_0", "hqo_quantize_q4_k"):
             getattr(L, name).argtypes = [_p, _i64, _i64, _p]
             getattr(L, name).restype = None
         L.hqo_quantize_i8_rows.argtypes = [_p, _i64, _i64, _p, _p]
         L.hqo_quantize_i8_rows.restype = None
-        for name in ("hqo_dequant_q8_0", "hqo_dequant_q4_0"):
+        for name in ("hqo_dequant_q8_0", "hqo_dequant_q4_0", "hqo_dequant_q4_k"):
             getattr(L, name).argtypes = [_p, _i64, _i64, _p]
             getattr(L, name).restype = None
-        for name in ("hqo_matvec_q8_0", "hqo_matvec_q4_0"):
+        for name in ("hqo_matvec_q8_0", "hqo_matvec_q4_0", "hqo_matvec_q4_k"):
             getattr(L, name).argtypes = [_p, _p, _i64, _i64, _int, _p, _p]
             getattr(L, name).restype = None
         L.hqo_matvec_rows.argtypes = [_int, _p, _p, _i64, _i64, _i64, _i64, _int, _p, _p]
@@ -77,7 +77,7 @@ def lib() -> ctypes.CDLL:
         L.hqo_silu.restype = ctypes.c_double
         L.hqo_swiglu_pairs.argtypes = [_p, _i64, _p]
         L.hqo_moe_combine.argtypes = [_p, _p, _p, _int, _int, _i64, _p, _p]
-        L.hqo_lora_delta.restype = None
+        L.hqo_lora_delta.restype = ctypes.c_int
         L.hqo_version.restype = _int
         _LIB = L
     return _LIB
@@ -102,7 +102,16 @@ def float_to_half(f: float) -> int:
 
 Q8_0_BYTES = 34
 Q4_0_BYTES = 18
+Q4_K_BYTES = 144
 QK = 32
+QK_K = 256
+# format name -> (weights per block, bytes per block, code of the C matvec_rows)
+FORMATS = {"q8_0": (QK, Q8_0_BYTES, 8), "q4_0": (QK, Q4_0_BYTES, 4), "q4_k": (QK_K, Q4_K_BYTES, ord("K"))}
+
+
+def row_bytes(fmt: str, cols: int) -> int:
+    qk, bb, _ = FORMATS[fmt]
+    return cols // qk * bb
 
 
 def quantize_q8_0(W: np.ndarray) -> np.ndarray:
@@ -125,6 +134,21 @@ def quantize_q4_0(W: np.ndarray) -> np.ndarray:
     return out
 
 
+def quantize_q4_k(W: np.ndarray) -> np.ndarray:
+    """fp32 [rows][cols] -> uint8 [rows][cols/256*144] (ggml Q4_K super-blocks,
+    encoded by the oracle's min/max reading; cols % 256 == 0)."""
+    W = np.ascontiguousarray(W, dtype=np.float32)
+    rows, cols = W.shape
+    assert cols % QK_K == 0
+    out = np.empty((rows, cols // QK_K * Q4_K_BYTES), dtype=np.uint8)
+    lib().hqo_quantize_q4_k(_ptr(W), rows, cols, _ptr(out))
+    return out
+
+
+def quantize(fmt: str, W: np.ndarray) -> np.ndarray:
+    return {"q8_0": quantize_q8_0, "q4_0": quantize_q4_0, "q4_k": quantize_q4_k}[fmt](W)
+
+
 def quantize_i8_rows(W: np.ndarray):
     """fp32 [rows][cols] -> (int8 [rows][cols], fp32 scale [rows])."""
     W = np.ascontiguousarray(W, dtype=np.float32)
@@ -138,7 +162,7 @@ def quantize_i8_rows(W: np.ndarray):
 def dequant(fmt: str, blocks: np.ndarray, rows: int, cols: int) -> np.ndarray:
     blocks = np.ascontiguousarray(blocks, dtype=np.uint8)
     out = np.empty((rows, cols), dtype=np.float64)
-    fn = lib().hqo_dequant_q8_0 if fmt == "q8_0" else lib().hqo_dequant_q4_0
+    fn = {"q8_0": lib().hqo_dequant_q8_0, "q4_0": lib().hqo_dequant_q4_0, "q4_k": lib().hqo_dequant_q4_k}[fmt]
     fn(_ptr(blocks), rows, cols, _ptr(out))
     return out
 
@@ -152,7 +176,7 @@ def matvec(fmt: str, blocks: np.ndarray, x: np.ndarray, rows: int, cols: int):
     n_vec = x.shape[0]
     y = np.empty((n_vec, rows), dtype=np.float64)
     T = np.empty((n_vec, rows), dtype=np.float64)
-    fn = lib().hqo_matvec_q8_0 if fmt == "q8_0" else lib().hqo_matvec_q4_0
+    fn = {"q8_0": lib().hqo_matvec_q8_0, "q4_0": lib().hqo_matvec_q4_0, "q4_k": lib().hqo_matvec_q4_k}[fmt]
     fn(_ptr(blocks), _ptr(x), rows, cols, n_vec, _ptr(y), _ptr(T))
     return y, T
 
@@ -165,7 +189,7 @@ def matvec_rows(fmt: str, blocks: np.ndarray, x: np.ndarray, rows: int, cols: in
     n_vec = x.shape[0]
     y = np.zeros((n_vec, rows), dtype=np.float64)
     T = np.zeros((n_vec, rows), dtype=np.float64)
-    lib().hqo_matvec_rows(8 if fmt == "q8_0" else 4, _ptr(blocks), _ptr(x), row_lo,
+    lib().hqo_matvec_rows(FORMATS[fmt][2], _ptr(blocks), _ptr(x), row_lo,
                           row_hi, rows, cols, n_vec, _ptr(y), _ptr(T))
     return y[:, row_lo:row_hi], T[:, row_lo:row_hi]
 
@@ -273,7 +297,10 @@ def lora_delta(A: np.ndarray, B: np.ndarray, x: np.ndarray, scale: float):
     n_vec = x.shape[0]
     delta = np.empty((n_vec, rows), dtype=np.float64)
     T = np.empty((n_vec, rows), dtype=np.float64)
-    lib().hqo_lora_delta(_ptr(A), _ptr(B), _ptr(x), float(scale), rank, rows, cols, n_vec, _ptr(delta), _ptr(T))
+    rc = lib().hqo_lora_delta(_ptr(A), _ptr(B), _ptr(x), float(scale), rank, rows, cols, n_vec, _ptr(delta),
+                              _ptr(T))
+    if rc != 0:
+        raise ValueError(f"hqo_lora_delta failed (rank {rank})")
     return delta, T
 
 

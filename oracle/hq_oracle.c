@@ -23,12 +23,16 @@
  *          all integer), section "Gaps vs the current toy engine", item 3,
  *          and section "Architecture" (the feed-forward is SwiGLU(gate, up,
  *          down)).
+ *   [NST]  also section "Ported Versus Novel": every format, Q4_K included, is
+ *          taken verbatim from ggml.  Q4_K is therefore ggml's super-block of
+ *          256 weights in 144 bytes: fp16 d, fp16 dmin, 12 bytes packing eight
+ *          6-bit sub-block scales and eight 6-bit sub-block mins, then 128
+ *          bytes of 4-bit quants; w = d * sc_j * q - dmin * m_j for sub-block j.
  *   [EPS]  also paragraph "MoE is the cheapest-per-quality tier" (a sparsely
  *          gated mixture: the output is the gate-weighted sum of the chosen
  *          experts' outputs).
  *
- * Readings taken where the pages are silent (each one is listed in the design
- * notes): fp16 scale rounded to nearest-even from an fp32 d; q = round(w/d)
+ * Readings taken where the pages are silent: fp16 scale rounded to nearest-even from an fp32 d; q = round(w/d)
  * with round-half-away-from-zero in fp32; Q4_0 nibble n = min(15, floor(w/d +
  * 8.5)) with d = (signed absmax)/-8 and ggml's nibble order (byte j holds
  * element j low, element j+16 high); all-zero blocks give d = 0 (Q4_0: -0.0,
@@ -40,12 +44,15 @@
  * Build with -ffp-contract=off: no fused multiply-add may change a result.
  */
 #include <stdint.h>
+#include <stdlib.h>
 #include <string.h>
 #include <math.h>
 
 #define HQO_QK 32             /* weights per block (both formats)          */
 #define HQO_Q8_0_BYTES 34     /* 2 B fp16 scale + 32 x int8                */
 #define HQO_Q4_0_BYTES 18     /* 2 B fp16 scale + 16 B of nibbles          */
+#define HQO_QK_K 256          /* Q4_K: weights per super-block              */
+#define HQO_Q4_K_BYTES 144    /* 2 B d + 2 B dmin + 12 B scales/mins + 128 B nibbles */
 
 /* ------------------------------------------------------------------------ */
 /* IEEE 754 binary16 <-> binary32, written from the format definition:       */
@@ -180,6 +187,98 @@ void hqo_quantize_q4_0(const float *W, int64_t rows, int64_t cols, uint8_t *out)
     }
 }
 
+/* Q4_K sub-block j (0..7) of a super-block: its 6-bit scale and 6-bit min
+ * from the 12 packed bytes.  Sub-blocks 0..3 keep both in the low 6 bits of
+ * bytes j and j+4; sub-blocks 4..7 keep their low 4 bits in the two nibbles of
+ * byte j+4 (scale low, min high) and their top 2 bits in the top 2 bits of
+ * bytes j-4 (scale) and j (min). */
+static void q4k_scale_min(const uint8_t *s12, int j, int *sc, int *m)
+{
+    if (j < 4) {
+        *sc = s12[j] & 63;
+        *m = s12[j + 4] & 63;
+    } else {
+        *sc = (s12[j + 4] & 0x0f) | ((s12[j - 4] >> 6) << 4);
+        *m = (s12[j + 4] >> 4) | ((s12[j] >> 6) << 4);
+    }
+}
+
+/* Element e (0..255) of a Q4_K super-block: sub-block j = e / 32 reads the
+ * quant bytes of group j / 2 (32 bytes); an even sub-block takes the low
+ * nibbles of that group, an odd one the high nibbles. */
+static int q4k_quant(const uint8_t *blk, int e)
+{
+    int j = e / 32, l = e % 32;
+    uint8_t b = blk[16 + 32 * (j / 2) + l];
+    return (j & 1) ? (b >> 4) : (b & 0x0f);
+}
+
+/* Q4_K encoder (the pages print none; this is a plain min/max reading of the
+ * format).  Per sub-block of 32: mn = min(0, min w), mx = max w, scale =
+ * (mx - mn) / 15 and min = -mn (fp32).  d = max scale / 63 and dmin = max min
+ * / 63 (fp32; the maxima are taken from +0 upwards), stored fp16 (RNE).  sc_j = min(63, round(scale_j * (63 / max
+ * scale))), m_j likewise with the mins (0 when the maximum is 0).  Then, with
+ * the stored fp16 values, a = d * sc_j and b = dmin * m_j (fp32, exact), q =
+ * clamp(round((w + b) / a), 0, 15) (fp32, half away from zero), q = 0 when
+ * a == 0.  Rows are cols / 256 super-blocks, no padding. */
+void hqo_quantize_q4_k(const float *W, int64_t rows, int64_t cols, uint8_t *out)
+{
+    int64_t nsb = cols / HQO_QK_K;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const float *w = W + r * cols + sb * HQO_QK_K;
+            uint8_t *blk = out + (r * nsb + sb) * HQO_Q4_K_BYTES;
+            float scale[8], minv[8], max_scale = 0.0f, max_min = 0.0f;
+            for (int j = 0; j < 8; ++j) {
+                float mn = w[32 * j], mx = w[32 * j];
+                for (int l = 1; l < 32; ++l) {
+                    if (w[32 * j + l] < mn) mn = w[32 * j + l];
+                    if (w[32 * j + l] > mx) mx = w[32 * j + l];
+                }
+                if (mn > 0.0f) mn = 0.0f;
+                scale[j] = (mx - mn) / 15.0f;
+                minv[j] = -mn;
+                if (scale[j] > max_scale) max_scale = scale[j];
+                if (minv[j] > max_min) max_min = minv[j];
+            }
+            uint16_t dh = hqo_float_to_half_rne(max_scale / 63.0f);
+            uint16_t mh = hqo_float_to_half_rne(max_min / 63.0f);
+            float inv_s = max_scale > 0.0f ? 63.0f / max_scale : 0.0f;
+            float inv_m = max_min > 0.0f ? 63.0f / max_min : 0.0f;
+            int sc[8], mq[8];
+            for (int j = 0; j < 8; ++j) {
+                sc[j] = clamp_i32((int32_t)roundf(scale[j] * inv_s), 0, 63);
+                mq[j] = clamp_i32((int32_t)roundf(minv[j] * inv_m), 0, 63);
+            }
+            blk[0] = (uint8_t)(dh & 0xff);
+            blk[1] = (uint8_t)(dh >> 8);
+            blk[2] = (uint8_t)(mh & 0xff);
+            blk[3] = (uint8_t)(mh >> 8);
+            for (int j = 0; j < 4; ++j) {
+                blk[4 + j] = (uint8_t)(sc[j] | ((sc[j + 4] >> 4) << 6));
+                blk[8 + j] = (uint8_t)(mq[j] | ((mq[j + 4] >> 4) << 6));
+                blk[12 + j] = (uint8_t)((sc[j + 4] & 0x0f) | ((mq[j + 4] & 0x0f) << 4));
+            }
+            float dq = hqo_half_to_float(dh), mqf = hqo_half_to_float(mh);
+            int q[HQO_QK_K];
+            for (int j = 0; j < 8; ++j) {
+                float a = dq * (float)sc[j], b = mqf * (float)mq[j];
+                for (int l = 0; l < 32; ++l) {
+                    int32_t v = 0;
+                    if (a > 0.0f) {
+                        float t = (w[32 * j + l] + b) / a;
+                        v = clamp_i32((int32_t)roundf(t), 0, 15);
+                    }
+                    q[32 * j + l] = v;
+                }
+            }
+            for (int g = 0; g < 4; ++g)
+                for (int l = 0; l < 32; ++l)
+                    blk[16 + 32 * g + l] = (uint8_t)(q[64 * g + l] | (q[64 * g + 32 + l] << 4));
+        }
+    }
+}
+
 /* Per-output-channel symmetric int8 ([ZEN] "Quantization recipe"):
  * s[o] = max|W[o,:]| / 127 (fp32); Wq[o,j] = round(W[o,j] / s[o]) (fp32,
  * half away from zero) clamped to [-127,127]; s[o] == 0 gives 0.  With
@@ -238,6 +337,27 @@ void hqo_dequant_q4_0(const uint8_t *bytes, int64_t rows, int64_t cols, double *
         }
 }
 
+/* Q4_K: w = d * sc_j * q - dmin * m_j (f64, exact for the stored values). */
+static double q4k_weight(const uint8_t *blk, int e)
+{
+    int sc, m;
+    q4k_scale_min(blk + 4, e / 32, &sc, &m);
+    double d = (double)hqo_half_to_float(load_u16le(blk));
+    double dmin = (double)hqo_half_to_float(load_u16le(blk + 2));
+    return d * (double)sc * (double)q4k_quant(blk, e) - dmin * (double)m;
+}
+
+void hqo_dequant_q4_k(const uint8_t *bytes, int64_t rows, int64_t cols, double *Wd)
+{
+    int64_t nsb = cols / HQO_QK_K;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t sb = 0; sb < nsb; ++sb) {
+            const uint8_t *blk = bytes + (r * nsb + sb) * HQO_Q4_K_BYTES;
+            for (int e = 0; e < HQO_QK_K; ++e)
+                Wd[r * cols + sb * HQO_QK_K + e] = q4k_weight(blk, e);
+        }
+}
+
 /* ------------------------------------------------------------------------ */
 /* Float matvecs: y[v][i] = sum_j w_deq[i][j] * x[v][j], in f64, plus        */
 /* T[v][i] = sum_j |w_deq[i][j] * x[v][j]|.  x is [n_vec][cols], y and T are */
@@ -248,6 +368,24 @@ static void matvec_rows(int fmt, const uint8_t *bytes, const float *x,
                         int64_t row_lo, int64_t row_hi, int64_t rows, int64_t cols,
                         int n_vec, double *y, double *T)
 {
+    if (fmt == 'K') {                          /* Q4_K super-blocks */
+        int64_t nsb = cols / HQO_QK_K;
+        for (int64_t i = row_lo; i < row_hi; ++i)
+            for (int v = 0; v < n_vec; ++v) {
+                double acc = 0.0, aabs = 0.0;
+                for (int64_t sb = 0; sb < nsb; ++sb) {
+                    const uint8_t *blk = bytes + (i * nsb + sb) * HQO_Q4_K_BYTES;
+                    for (int e = 0; e < HQO_QK_K; ++e) {
+                        double p = q4k_weight(blk, e) * (double)x[(int64_t)v * cols + sb * HQO_QK_K + e];
+                        acc += p;
+                        aabs += fabs(p);
+                    }
+                }
+                y[(int64_t)v * rows + i] = acc;
+                if (T) T[(int64_t)v * rows + i] = aabs;
+            }
+        return;
+    }
     int64_t nb = cols / HQO_QK;
     int64_t bpb = fmt == 8 ? HQO_Q8_0_BYTES : HQO_Q4_0_BYTES;
     for (int64_t i = row_lo; i < row_hi; ++i) {
@@ -284,7 +422,14 @@ void hqo_matvec_q4_0(const uint8_t *W, const float *x, int64_t rows, int64_t col
     matvec_rows(4, W, x, 0, rows, rows, cols, n_vec, y, T);
 }
 
-/* Rows [row_lo, row_hi) only, for sampled checks at full size. */
+void hqo_matvec_q4_k(const uint8_t *W, const float *x, int64_t rows, int64_t cols,
+                     int n_vec, double *y, double *T)
+{
+    matvec_rows('K', W, x, 0, rows, rows, cols, n_vec, y, T);
+}
+
+/* Rows [row_lo, row_hi) only, for sampled checks at full size (fmt 8: Q8_0,
+ * 4: Q4_0, 'K': Q4_K). */
 void hqo_matvec_rows(int fmt, const uint8_t *W, const float *x, int64_t row_lo,
                      int64_t row_hi, int64_t rows, int64_t cols, int n_vec,
                      double *y, double *T)
@@ -413,14 +558,20 @@ float hqo_bf16_to_float(uint16_t h)
     return f;
 }
 
-void hqo_lora_delta(const uint16_t *A, const uint16_t *B, const float *x, double scale,
-                    int64_t rank, int64_t rows, int64_t cols, int64_t n_vec,
-                    double *delta, double *T)
+int hqo_lora_delta(const uint16_t *A, const uint16_t *B, const float *x, double scale,
+                   int64_t rank, int64_t rows, int64_t cols, int64_t n_vec,
+                   double *delta, double *T)
 {
-    double u[64], ua[64];                  /* the adapter's rank is at most 64 */
+    /* any rank >= 1: u = A x and its magnitudes live in heap buffers of rank
+       entries; returns -1 (and writes nothing) if rank < 1 or they cannot be
+       allocated, 0 otherwise */
+    if (rank < 1) return -1;
+    double *u = (double *)malloc((size_t)rank * sizeof(double));
+    double *ua = (double *)malloc((size_t)rank * sizeof(double));
+    if (!u || !ua) { free(u); free(ua); return -1; }
     for (int64_t v = 0; v < n_vec; ++v) {
         /* the bracket (A x) first, as the Lemma writes it */
-        for (int64_t k = 0; k < rank && k < 64; ++k) {
+        for (int64_t k = 0; k < rank; ++k) {
             u[k] = 0.0;
             ua[k] = 0.0;
             for (int64_t j = 0; j < cols; ++j) {
@@ -432,7 +583,7 @@ void hqo_lora_delta(const uint16_t *A, const uint16_t *B, const float *x, double
         /* then B_A applied to it, and the scale */
         for (int64_t i = 0; i < rows; ++i) {
             double acc = 0.0, mag = 0.0;
-            for (int64_t k = 0; k < rank && k < 64; ++k) {
+            for (int64_t k = 0; k < rank; ++k) {
                 double b = (double)hqo_bf16_to_float(B[i * rank + k]);
                 acc += b * u[k];
                 mag += fabs(b) * ua[k];
@@ -441,6 +592,9 @@ void hqo_lora_delta(const uint16_t *A, const uint16_t *B, const float *x, double
             T[v * rows + i] = fabs(scale) * mag;
         }
     }
+    free(u);
+    free(ua);
+    return 0;
 }
 
 /* ------------------------------------------------------------------------ */

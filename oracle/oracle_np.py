@@ -42,9 +42,49 @@ def dequant_q4_0(blocks: np.ndarray, rows: int, cols: int) -> np.ndarray:
     return (q * d[:, :, None]).reshape(rows, cols)
 
 
+QK_K = 256
+
+
+def q4_k_fields(blocks: np.ndarray, rows: int, cols: int):
+    """(d, dmin, sc, m, q) of every Q4_K super-block, read with NumPy: d, dmin
+    f64 [rows][nsb]; sc, m int [rows][nsb][8]; q int [rows][nsb][256].  The
+    six-bit fields are gathered from their bit positions: sub-block j < 4 has
+    sc = bits 0-5 of byte 4+j and m = bits 0-5 of byte 8+j; j >= 4 has the low
+    four bits of sc / m in the low / high nibble of byte 8+j and the top two
+    bits in bits 6-7 of byte j (sc) / byte 4+j (m), counting from byte 4."""
+    nsb = cols // QK_K
+    b = np.ascontiguousarray(blocks, dtype=np.uint8).reshape(rows, nsb, 144).astype(np.int64)
+    d = b[:, :, 0:2].astype(np.uint8).copy().view(np.float16)[..., 0].astype(np.float64)
+    dmin = b[:, :, 2:4].astype(np.uint8).copy().view(np.float16)[..., 0].astype(np.float64)
+    s12 = b[:, :, 4:16]
+    sc = np.empty((rows, nsb, 8), np.int64)
+    m = np.empty((rows, nsb, 8), np.int64)
+    sc[..., :4] = s12[..., 0:4] % 64
+    m[..., :4] = s12[..., 4:8] % 64
+    sc[..., 4:] = (s12[..., 8:12] % 16) + 16 * (s12[..., 0:4] // 64)
+    m[..., 4:] = (s12[..., 8:12] // 16) + 16 * (s12[..., 4:8] // 64)
+    qs = b[:, :, 16:].reshape(rows, nsb, 4, 32)                 # 4 groups of 32 bytes
+    lo, hi = qs % 16, qs // 16                                  # sub-blocks 2g and 2g+1
+    q = np.stack([lo, hi], axis=3).reshape(rows, nsb, 256)      # [g][lo|hi][32] = element order
+    return d, dmin, sc, m, q
+
+
+def dequant_q4_k(blocks: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    d, dmin, sc, m, q = q4_k_fields(blocks, rows, cols)
+    nsb = cols // QK_K
+    sub = np.repeat(np.arange(8), 32)                           # sub-block of each element
+    a = d[:, :, None] * sc[:, :, sub]
+    c = dmin[:, :, None] * m[:, :, sub]
+    return (a * q - c).reshape(rows, nsb * QK_K)
+
+
+def dequant(fmt: str, blocks: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    return {"q8_0": dequant_q8_0, "q4_0": dequant_q4_0, "q4_k": dequant_q4_k}[fmt](blocks, rows, cols)
+
+
 def matvec(fmt: str, blocks: np.ndarray, x: np.ndarray, rows: int, cols: int):
     """Brute force: (dequant(bytes) @ x^T)^T in f64, and T = |W| @ |x|."""
-    Wd = dequant_q8_0(blocks, rows, cols) if fmt == "q8_0" else dequant_q4_0(blocks, rows, cols)
+    Wd = dequant(fmt, blocks, rows, cols)
     X = np.asarray(x, dtype=np.float32).reshape(-1, cols).astype(np.float64)
     y = X @ Wd.T
     T = np.abs(X) @ np.abs(Wd).T
@@ -145,6 +185,51 @@ def quantize_q4_0(W: np.ndarray) -> np.ndarray:
     out[:, :, 0:2] = d.astype(np.float16).view(np.uint8).reshape(rows, nb, 2)
     out[:, :, 2:] = n[:, :, :16] | (n[:, :, 16:] << 4)
     return out.reshape(rows, nb * 18)
+
+
+def quantize_q4_k(W: np.ndarray) -> np.ndarray:
+    """The Q4_K min/max encoder restated with NumPy fp32 arrays: per sub-block
+    scale = (max - min(0, min)) / 15 and min = -min(0, min); d, dmin = the
+    largest of each / 63 stored fp16; 6-bit sc, m by rounding against the
+    largest; q = round((w + dmin m) / (d sc)) clamped to [0, 15]."""
+    W = np.asarray(W, dtype=np.float32)
+    rows, cols = W.shape
+    nsb = cols // QK_K
+    w = W.reshape(rows, nsb, 8, 32)
+    mn = np.minimum(w.min(axis=3), np.float32(0))
+    mx = w.max(axis=3)
+    scale = ((mx - mn) / np.float32(15)).astype(np.float32)
+    minv = (-mn).astype(np.float32)
+    ms = scale.max(axis=2)
+    mm = minv.max(axis=2)
+    # the largest scale and min, taken from +0 upwards (an all-zero super-block
+    # has min -0: its stored dmin is +0, as the running maximum from 0 gives)
+    ms = np.where(ms > 0, ms, np.float32(0)).astype(np.float32)
+    mm = np.where(mm > 0, mm, np.float32(0)).astype(np.float32)
+    dh = (ms / np.float32(63)).astype(np.float32).astype(np.float16)
+    mh = (mm / np.float32(63)).astype(np.float32).astype(np.float16)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        inv_s = np.where(ms > 0, np.float32(63) / ms, np.float32(0)).astype(np.float32)
+        inv_m = np.where(mm > 0, np.float32(63) / mm, np.float32(0)).astype(np.float32)
+
+    def rnd(t):                                              # half away from zero
+        return np.sign(t) * np.floor(np.abs(t) + np.float32(0.5))
+    sc = np.clip(rnd((scale * inv_s[:, :, None]).astype(np.float32)), 0, 63).astype(np.int64)
+    m = np.clip(rnd((minv * inv_m[:, :, None]).astype(np.float32)), 0, 63).astype(np.int64)
+    a = (dh.astype(np.float32)[:, :, None] * sc.astype(np.float32)).astype(np.float32)
+    b = (mh.astype(np.float32)[:, :, None] * m.astype(np.float32)).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        t = ((w + b[..., None]).astype(np.float32) / a[..., None]).astype(np.float32)
+    q = np.where(a[..., None] > 0, np.clip(rnd(t), 0, 15), 0).astype(np.int64)   # [rows][nsb][8][32]
+    out = np.zeros((rows, nsb, 144), dtype=np.uint8)
+    out[:, :, 0:2] = dh.view(np.uint8).reshape(rows, nsb, 2)
+    out[:, :, 2:4] = mh.view(np.uint8).reshape(rows, nsb, 2)
+    out[:, :, 4:8] = sc[..., :4] + 64 * (sc[..., 4:] // 16)
+    out[:, :, 8:12] = m[..., :4] + 64 * (m[..., 4:] // 16)
+    out[:, :, 12:16] = (sc[..., 4:] % 16) + 16 * (m[..., 4:] % 16)
+    qg = q.reshape(rows, nsb, 4, 2, 32)
+    out[:, :, 16:] = (qg[:, :, :, 0, :] + 16 * qg[:, :, :, 1, :]).reshape(rows, nsb, 128)
+    return out.reshape(rows, nsb * 144)
 
 
 # ----------------------------------------------------------- exact integer rules

@@ -56,6 +56,28 @@ def test_brute_force_against_numpy():
             assert np.allclose(T, T_ref, rtol=1e-12, atol=1e-14)
 
 
+def test_ranks_beyond_the_kernel_limit():
+    # the oracle has no rank limit of its own: ranks 65 and 100 (above the
+    # kernels' 64) still equal the NumPy statement term for term, and a rank
+    # below 1 is refused rather than answered
+    for seed, rank in ((11, 65), (12, 100)):
+        A, B, x = _case(seed, rank, 9, 64, 2)
+        d, T = oracle.lora_delta(A, B, x, 0.75)
+        d_ref, T_ref = oracle_np.lora_delta(A, B, x, 0.75)
+        assert np.allclose(d, d_ref, rtol=1e-12, atol=1e-14)
+        assert np.allclose(T, T_ref, rtol=1e-12, atol=1e-14)
+        # the last adapter row matters: dropping it changes the answer
+        d_cut, _ = oracle_np.lora_delta(A[:64], B[:, :64], x, 0.75)
+        assert not np.allclose(d, d_cut, rtol=1e-9, atol=0)
+    try:
+        oracle.lora_delta(np.zeros((0, 32), np.uint16), np.zeros((3, 0), np.uint16),
+                          np.zeros((1, 32), np.float32), 1.0)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("rank 0 was accepted")
+
+
 def test_closed_forms():
     rank, rows, cols = 3, 4, 8
     x = np.arange(1, 2 * cols + 1, dtype=np.float32).reshape(2, cols)

@@ -48,6 +48,18 @@ MUTANTS = {
                                    "double wk = (double)w[k * n_vec + t];"),
     "lora_scale_dropped": ("delta[v * rows + i] = scale * acc;", "delta[v * rows + i] = acc;"),
     "bf16_shift_15": ("uint32_t u = (uint32_t)h << 16;", "uint32_t u = (uint32_t)h << 15;"),
+    "q4k_sub_block_nibbles_swapped": ("return (j & 1) ? (b >> 4) : (b & 0x0f);",
+                                      "return (j & 1) ? (b & 0x0f) : (b >> 4);"),
+    "q4k_interleaved_nibbles": ("uint8_t b = blk[16 + 32 * (j / 2) + l];\n    return (j & 1) ? (b >> 4) : (b & 0x0f);",
+                                "uint8_t b = blk[16 + e / 2];\n    (void)j; (void)l;\n    return (e & 1) ? (b >> 4) : (b & 0x0f);"),
+    "q4k_min_term_sign": ("return d * (double)sc * (double)q4k_quant(blk, e) - dmin * (double)m;",
+                          "return d * (double)sc * (double)q4k_quant(blk, e) + dmin * (double)m;"),
+    "q4k_scale_high_bits_wrong_byte": ("*sc = (s12[j + 4] & 0x0f) | ((s12[j - 4] >> 6) << 4);",
+                                       "*sc = (s12[j + 4] & 0x0f) | ((s12[j] >> 6) << 4);"),
+    "q4k_d_dmin_swapped": ("double d = (double)hqo_half_to_float(load_u16le(blk));\n    double dmin = (double)hqo_half_to_float(load_u16le(blk + 2));",
+                           "double d = (double)hqo_half_to_float(load_u16le(blk + 2));\n    double dmin = (double)hqo_half_to_float(load_u16le(blk));"),
+    "q4k_encoder_min_not_clamped": ("if (mn > 0.0f) mn = 0.0f;\n", "\n"),
+    "q4k_encoder_scale_over_16": ("scale[j] = (mx - mn) / 15.0f;", "scale[j] = (mx - mn) / 16.0f;"),
 }
 
 
@@ -62,11 +74,11 @@ def _build_mutant(tmp_path, name):
                     "-o", str(so), str(p), "-lm"], check=True)
     L = ctypes.CDLL(str(so))
     vp, i64, ci = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
-    for fn in ("hqo_quantize_q8_0", "hqo_quantize_q4_0"):
+    for fn in ("hqo_quantize_q8_0", "hqo_quantize_q4_0", "hqo_quantize_q4_k"):
         getattr(L, fn).argtypes = [vp, i64, i64, vp]
-    for fn in ("hqo_dequant_q8_0", "hqo_dequant_q4_0"):
+    for fn in ("hqo_dequant_q8_0", "hqo_dequant_q4_0", "hqo_dequant_q4_k"):
         getattr(L, fn).argtypes = [vp, i64, i64, vp]
-    for fn in ("hqo_matvec_q8_0", "hqo_matvec_q4_0"):
+    for fn in ("hqo_matvec_q8_0", "hqo_matvec_q4_0", "hqo_matvec_q4_k"):
         getattr(L, fn).argtypes = [vp, vp, i64, i64, ci, vp, vp]
     L.hqo_srdhm.argtypes = [ctypes.c_int32, ctypes.c_int32]
     L.hqo_srdhm.restype = ctypes.c_int32
@@ -127,6 +139,38 @@ def _pins_fail(L, golden_dir):
         ref = oracle_np.dequant_q8_0(blocks, rows, cols) if fmt == "q8_0" else oracle_np.dequant_q4_0(blocks, rows, cols)
         if not np.array_equal(Wd, ref):
             failed.append("dequant:" + fmt)
+    # Q4_K: the hand-worked super-blocks, the NumPy encoder and decoder, brute force
+    from test_oracle_q4_k import _golden as q4k_golden, _block_bytes as q4k_bytes, _special_weights
+    gk = q4k_golden()
+    blk = q4k_bytes(gk["q4_k_decode"])
+    wd = np.empty(256)
+    L.hqo_dequant_q4_k(ptr(blk), 1, 256, ptr(wd))
+    for e in range(256):
+        j, l = divmod(e, 32)
+        q = l % 16 if j % 2 == 0 else 15 - l % 16
+        if wd[e] != gk["q4_k_decode"]["d"] * gk["q4_k_decode"]["sc"][j] * q - gk["q4_k_decode"]["dmin"] * gk["q4_k_decode"]["m"][j]:
+            failed.append("golden:q4_k_decode")
+            break
+    ramp = np.tile(np.array([(l % 16) - 7.5 for l in range(32)], np.float32), 8).reshape(1, 256)
+    out = np.empty(144, np.uint8)
+    L.hqo_quantize_q4_k(ptr(ramp), 1, 256, ptr(out))
+    if out.tobytes() != q4k_bytes(gk["q4_k_encode_ramp"]).tobytes():
+        failed.append("golden:q4_k_encode_ramp")
+    Wk = _special_weights(21, 512, 79)
+    out = np.empty((21, 288), np.uint8)
+    L.hqo_quantize_q4_k(ptr(Wk), 21, 512, ptr(out))
+    if not np.array_equal(out, oracle_np.quantize_q4_k(Wk)):
+        failed.append("quantizer:q4_k")
+    blocks = oracle.quantize_q4_k(Wk)
+    Wd = np.empty((21, 512))
+    L.hqo_dequant_q4_k(ptr(blocks), 21, 512, ptr(Wd))
+    if not np.array_equal(Wd, oracle_np.dequant_q4_k(blocks, 21, 512)):
+        failed.append("dequant:q4_k")
+    xk = synthetic.activations(synthetic.rng(80), 3, 512)
+    y = np.empty((3, 21)); T = np.empty((3, 21))
+    L.hqo_matvec_q4_k(ptr(blocks), ptr(xk), 21, 512, 3, ptr(y), ptr(T))
+    if not np.allclose(y, oracle_np.matvec("q4_k", blocks, xk, 21, 512)[0], rtol=1e-12, atol=1e-12):
+        failed.append("brute:q4_k")
     # integer rules
     w = json.load(open(os.path.join(golden_dir, "gemmlowp_worked.json")))
     if any(L.hqo_srdhm(c["a"], c["b"]) != c["out"] for c in w["srdhm"]):
