@@ -53,6 +53,7 @@ WORKLOADS = {
     "8b-q8_0-unfused": ("dense", "8b-dense", "q8_0", False),
     "8b-q4_0": ("dense", "8b-dense", "q4_0", True),
     "8b-q4_0-unfused": ("dense", "8b-dense", "q4_0", False),
+    "8b-q4_k": ("dense", "8b-dense", "q4_k", True),
     "qwen3-0.6b-q8_0": ("dense", "qwen3-0.6b", "q8_0", True),
     "qwen3-0.6b-q8_0-unfused": ("dense", "qwen3-0.6b", "q8_0", False),
     "moe-q8_0": ("moe", "moe-128x8-hidden2048", "q8_0", True),
@@ -153,6 +154,8 @@ def workload_ops(name, n_vec, shape=None, fmt=None, seed=synthetic.SEED_BASE + 2
 def weight_bytes(fmt, rows, cols):
     if fmt == "i8":
         return rows * cols
+    if fmt == "q4_k":
+        return rows * (cols // 256) * 144
     return rows * (cols // 32) * (34 if fmt == "q8_0" else 18)
 
 
@@ -415,7 +418,7 @@ class Step:
             hq.hq_quantize_i8_rows(wf, wq, op_scale, op.rows, op.cols)
             self._last_scale = op_scale
             return wq
-        quant = hq.hq_quantize_q8_0 if op.fmt == "q8_0" else hq.hq_quantize_q4_0
+        quant = {"q8_0": hq.hq_quantize_q8_0, "q4_0": hq.hq_quantize_q4_0, "q4_k": hq.hq_quantize_q4_k}[op.fmt]
         rb = weight_bytes(op.fmt, 1, op.cols)
         n_mat = op.n_experts if op.kind == "moe" else 1
         wq = torch.empty((n_mat * op.rows, rb), dtype=torch.uint8, device=self.device)
@@ -452,7 +455,7 @@ class Step:
                 fn(self.W[i], self.x[i], A, B, LORA_SCALE, op.lora_rank, ws, self.y[i], op.rows, op.cols, n_vec,
                    stream=stream)
             elif op.kind == "dense":
-                fn = hq.hq_matvec_q8_0 if op.fmt == "q8_0" else hq.hq_matvec_q4_0
+                fn = {"q8_0": hq.hq_matvec_q8_0, "q4_0": hq.hq_matvec_q4_0, "q4_k": hq.hq_matvec_q4_k}[op.fmt]
                 fn(self.W[i], self.x[i], self.y[i], op.rows, op.cols, n_vec, stream=stream)
             elif op.kind == "moe" and op.epi == "swiglu":
                 hq.hq_moe_matvec_q8_0_swiglu(self.W[i], self.ids[i], self.x[i], op.x_per_slot, self.y[i],
@@ -558,7 +561,7 @@ class OracleSample:
             if op.kind == "dense":
                 r = min(op.rows, max(8, (1 << 22) // op.cols))
                 W = synthetic.weights(g, r, op.cols)
-                blocks = oracle.quantize_q8_0(W) if self.fmt == "q8_0" else oracle.quantize_q4_0(W)
+                blocks = oracle.quantize(self.fmt, W)
                 x = synthetic.activations(g, n_vec, op.cols)
                 self.calls.append(lambda b=blocks, x=x, r=r, c=op.cols: oracle.matvec(self.fmt, b, x, r, c))
                 self.pass_bytes += weight_bytes(self.fmt, r, op.cols)
@@ -651,7 +654,7 @@ def main():
     ap.add_argument("--n-vec", type=int, default=1)
     ap.add_argument("--shape", default=None,
                     help="time one matrix shape ROWSxCOLS instead of a decode token (profiling aid)")
-    ap.add_argument("--format", choices=["q8_0", "q4_0"], default="q8_0", help="format for --shape")
+    ap.add_argument("--format", choices=["q8_0", "q4_0", "q4_k"], default="q8_0", help="format for --shape")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--traffic-file", default=os.path.join(ROOT, "profiles", "dram_traffic.txt"),
@@ -832,7 +835,7 @@ def main():
                                      "unit": "TFLOP/s", "frac": round(tflops / fp32_peak, 4),
                                      "peak_source": line["fp32_roof"]["peak_basis"] +
                                      " (derived from unit counts and the sampled clock)"})
-    if fmt == "q4_0" and args.n_vec <= 2:
+    if fmt in ("q4_0", "q4_k") and args.n_vec <= 2:
         line["roofline"]["limiter"] = ("nibble decode issue rate (one and per weight on the ALU pipe, one ffma2 "
                                        "per two weights on the FMA pipe), not HBM")
     if not args.no_cpu_baseline and not args.shape:

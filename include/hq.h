@@ -73,6 +73,12 @@ typedef enum {
     HQ_ERR_DEVICE = -7        /* a kernel reported a fault word (hq_device_fault)  */
 } hq_status;
 
+/* Format codes taken by hq_debug_plan. */
+#define HQ_FMT_Q8_0 8
+#define HQ_FMT_Q4_0 4
+#define HQ_FMT_Q4_K 75      /* 'K' */
+#define HQ_FMT_I8 1
+
 /* Library version (major*10000 + minor*100 + patch). */
 int hq_version(void);
 
@@ -104,6 +110,28 @@ hq_status hq_matvec_q8_0(const void *W, const float *x, float *y,
  */
 hq_status hq_matvec_q4_0(const void *W, const float *x, float *y,
                          int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
+
+/*
+ * hq_matvec_q4_k -- as hq_matvec_q8_0 for Q4_K super-blocks: W is
+ * rows x (cols/256) x 144 bytes, 16-byte aligned, cols % 256 == 0
+ * (HQ_ERR_SHAPE otherwise).  A super-block is { fp16 d, fp16 dmin, uint8
+ * scales[12], uint8 qs[128] }: sub-block j (32 weights, j = 0..7) has a
+ * six-bit scale sc_j and min m_j -- for j < 4, sc_j = scales[j] & 63 and
+ * m_j = scales[j+4] & 63; for j >= 4, sc_j = (scales[j+4] & 15) |
+ * (scales[j-4] >> 6) << 4 and m_j = (scales[j+4] >> 4) | (scales[j] >> 6) << 4
+ * -- and its quants are the low (even j) or high (odd j) nibbles of
+ * qs[32*(j/2) .. +31]; w = d*sc_j*q - dmin*m_j.  Each weight is formed in fp32
+ * (one rounding) before it multiplies x, so the accuracy statement and the
+ * |x| < 2^100 precondition of hq_matvec_q8_0 hold unchanged.
+ * Source: "One Native Stack ...", sections "The Unified Quant Core" (Q4_K is
+ * one of the native formats) and "Ported Versus Novel" (formats taken
+ * verbatim from ggml, whose Q4_K super-block this is); "Economical Serving
+ * ...", subsection "One Quant-Agnostic Core, Not a Kernel-per-Quant Zoo"
+ * (the Q4_K decode kernel).
+ */
+hq_status hq_matvec_q4_k(const void *W, const float *x, float *y,
+                         int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
+
 
 /*
  * hq_matvec_q8_0_lora, hq_matvec_q4_0_lora -- the float matvec of the same
@@ -270,6 +298,18 @@ hq_status hq_quantize_q4_0(const float *W, void *out, int64_t rows, int64_t cols
                            hq_stream_t stream);
 hq_status hq_quantize_i8_rows(const float *W, int8_t *Wq, float *scale,
                               int64_t rows, int64_t cols, hq_stream_t stream);
+/*
+ * hq_quantize_q4_k -- fp32 W [rows][cols] (4-byte aligned) to Q4_K
+ * super-blocks in out (rows x cols/256 x 144 B, 16-byte aligned), cols % 256
+ * == 0.  The pages give no encoder; this one is a plain min/max reading, per
+ * sub-block of 32: mn = min(0, min w), scale = (max w - mn)/15, min = -mn;
+ * d = (largest scale)/63 and dmin = (largest min)/63 stored fp16 (RNE);
+ * sc = round(scale * 63/largest scale), m likewise (at most 63); then with
+ * a = d*sc and b = dmin*m from the stored values, q = round((w + b)/a)
+ * clamped to [0, 15] (0 when a == 0).  All in fp32, half away from zero.
+ * Source: "One Native Stack ...", section "Ported Versus Novel" (ggml's Q4_K).
+ */
+hq_status hq_quantize_q4_k(const float *W, void *out, int64_t rows, int64_t cols, hq_stream_t stream);
 
 /*
  * hq_requant_params -- HOST function: real multipliers M[i] in (0, 1) to
@@ -333,7 +373,7 @@ uint64_t hq_launch_count(void);
  * `num_sms` SMs and `smem_optin` bytes of opt-in shared memory per CTA, for a
  * kernel of `regs` registers per thread.  Pure host arithmetic: no device is
  * touched, so it also runs on a machine without a GPU.
- *   fmt : 8 (Q8_0), 4 (Q4_0) or 1 (int8).  cols : a multiple of 256 (int8:
+ *   fmt : 8 (Q8_0), 4 (Q4_0), 75 (Q4_K) or 1 (int8).  cols : a multiple of 256 (int8:
  *         128), the shapes the TMA-staged kernel serves.
  *   out : int64 [out_len >= HQ_PLAN_FIELDS], caller-owned host memory,
  *         filled with { policy (0 one owner per stage, 1 Q8_0 short rows,

@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     HQ_ERR_UNSUPPORTED, HQ_ERR_DEVICE, HQ_FAULT_WAIT_TIMEOUT, HQ_FAULT_EXPERT_ID,
     lib, lib_path, hq_version, hq_last_error,
     hq_matvec_q8_0, hq_matvec_q4_0, hq_matvec_i8_requant, hq_moe_matvec_q8_0,
+    hq_matvec_q4_k, hq_quantize_q4_k, FMT_CODES, QK_K, Q4_K_BLOCK_BYTES,
     hq_moe_matvec_q8_0_swiglu, hq_moe_matvec_q8_0_combine,
     hq_matvec_q8_0_lora, hq_matvec_q4_0_lora, hq_matvec_q8_0_lora_noalloc,
     hq_quantize_q8_0, hq_quantize_q4_0, hq_quantize_i8_rows, hq_requant_params,

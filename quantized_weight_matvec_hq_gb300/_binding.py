@@ -22,6 +22,10 @@ HQ_FAULT_EXPERT_ID = 2
 QK = 32
 Q8_0_BLOCK_BYTES = 34
 Q4_0_BLOCK_BYTES = 18
+QK_K = 256
+Q4_K_BLOCK_BYTES = 144
+# format codes of hq_debug_plan
+FMT_CODES = {"q8_0": 8, "q4_0": 4, "q4_k": 75, "i8": 1}
 
 _NAMES = {HQ_ERR_NULL: "HQ_ERR_NULL", HQ_ERR_SHAPE: "HQ_ERR_SHAPE", HQ_ERR_ALIGN: "HQ_ERR_ALIGN",
           HQ_ERR_NVEC: "HQ_ERR_NVEC", HQ_ERR_LAUNCH: "HQ_ERR_LAUNCH",
@@ -46,6 +50,8 @@ _SIGS = {
     "hq_last_error": ([], ctypes.c_char_p),
     "hq_matvec_q8_0": ([_vp, _vp, _vp, _i64, _i64, _int, _vp], _int),
     "hq_matvec_q4_0": ([_vp, _vp, _vp, _i64, _i64, _int, _vp], _int),
+    "hq_matvec_q4_k": ([_vp, _vp, _vp, _i64, _i64, _int, _vp], _int),
+    "hq_quantize_q4_k": ([_vp, _vp, _i64, _i64, _vp], _int),
     "hq_matvec_i8_requant": ([_vp, _vp, _vp, _vp, _vp, _i64, _i64, _int, _vp], _int),
     "hq_matvec_q8_0_lora": ([_vp, _vp, _vp, _vp, ctypes.c_float, _int, _vp, _vp, _i64, _i64, _int, _vp], _int),
     "hq_matvec_q4_0_lora": ([_vp, _vp, _vp, _vp, ctypes.c_float, _int, _vp, _vp, _i64, _i64, _int, _vp], _int),
@@ -115,7 +121,10 @@ def _check(status: int) -> int:
 
 
 def row_bytes(fmt: str, cols: int) -> int:
-    """Bytes of one quantized row: cols/32 blocks of 34 (Q8_0) or 18 (Q4_0) bytes."""
+    """Bytes of one quantized row: cols/32 blocks of 34 (Q8_0) or 18 (Q4_0)
+    bytes, or cols/256 super-blocks of 144 (Q4_K) bytes."""
+    if fmt == "q4_k":
+        return cols // QK_K * Q4_K_BLOCK_BYTES
     return cols // QK * (Q8_0_BLOCK_BYTES if fmt == "q8_0" else Q4_0_BLOCK_BYTES)
 
 
@@ -133,6 +142,14 @@ def hq_matvec_q8_0(W, x, y, rows: int, cols: int, n_vec: int, stream=None) -> in
 
 def hq_matvec_q4_0(W, x, y, rows: int, cols: int, n_vec: int, stream=None) -> int:
     return _check(lib().hq_matvec_q4_0(_addr(W), _addr(x), _addr(y), rows, cols, n_vec, _stream(stream)))
+
+
+def hq_matvec_q4_k(W, x, y, rows: int, cols: int, n_vec: int, stream=None) -> int:
+    return _check(lib().hq_matvec_q4_k(_addr(W), _addr(x), _addr(y), rows, cols, n_vec, _stream(stream)))
+
+
+def hq_quantize_q4_k(W, out, rows: int, cols: int, stream=None) -> int:
+    return _check(lib().hq_quantize_q4_k(_addr(W), _addr(out), rows, cols, _stream(stream)))
 
 
 def hq_matvec_q8_0_lora(W, x, lora_A, lora_B, scale: float, rank: int, workspace, y, rows: int, cols: int,

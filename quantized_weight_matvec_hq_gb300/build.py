@@ -16,9 +16,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libhq.so")
-# (source, extra defines, object name): the kernel file is compiled in four parts
+# (source, extra defines, object name): the kernel file is compiled in five parts
+# (Q8_0, Q4_0, int8 and helpers, MoE, Q4_K)
 SOURCES = [("hq_api.cu", [], "hq_api.o"), ("hq_quant.cu", [], "hq_quant.o")] + [
-    ("hq_kernels.cu", [f"-DHQ_PART={i}"], f"hq_kernels_{i}.o") for i in range(4)]
+    ("hq_kernels.cu", [f"-DHQ_PART={i}"], f"hq_kernels_{i}.o") for i in range(5)]
 HEADERS = ["hq_device.cuh", "hq_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",

@@ -143,6 +143,14 @@ hq_status hq_matvec_q4_0(const void *W, const float *x, float *y, int64_t rows, 
     return finish(launch_matvec_float_q4_0(W, x, y, rows, cols, n_vec, nullptr, (cudaStream_t)stream));
 }
 
+hq_status hq_matvec_q4_k(const void *W, const float *x, float *y, int64_t rows, int64_t cols,
+                         int n_vec, hq_stream_t stream) {
+    hq_status st = check_float_matvec(W, x, y, rows, cols, n_vec);
+    if (st != HQ_OK) return st;
+    if (cols % 256 != 0) return set_error(HQ_ERR_SHAPE, "Q4_K needs cols %% 256 == 0 (cols = %lld)", (long long)cols);
+    return finish(launch_matvec_float_q4_k(W, x, y, rows, cols, n_vec, nullptr, (cudaStream_t)stream));
+}
+
 // The float matvec plus the QLoRA adapter term: u = A x into the caller's
 // workspace, then the matvec adds scale * B u as it stores each output.
 static hq_status matvec_lora(int fmt, const void *W, const float *x, const uint16_t *A, const uint16_t *B,
@@ -158,7 +166,7 @@ static hq_status matvec_lora(int fmt, const void *W, const float *x, const uint1
     cudaStream_t s = (cudaStream_t)stream;
     st = launch_lora_down(A, x, workspace, rank, cols, n_vec, s);
     if (st != HQ_OK) return st;
-    LoraArgs l;
+    MatvecExtras l;
     l.B = B;
     l.u = workspace;
     l.scale = scale;
@@ -203,8 +211,9 @@ hq_status hq_debug_plan(int fmt, int n_vec, int64_t rows, int64_t cols, int num_
     switch (fmt) {
         case 8: return debug_plan_float_q8_0(n_vec, rows, cols, num_sms, smem_optin, regs, out);
         case 4: return debug_plan_float_q4_0(n_vec, rows, cols, num_sms, smem_optin, regs, out);
+        case HQ_FMT_Q4_K: return debug_plan_float_q4_k(n_vec, rows, cols, num_sms, smem_optin, regs, out);
         case 1: return debug_plan_i8(n_vec, rows, cols, num_sms, smem_optin, regs, out);
-        default: return set_error(HQ_ERR_UNSUPPORTED, "fmt %d: 8 (Q8_0), 4 (Q4_0) or 1 (int8)", fmt);
+        default: return set_error(HQ_ERR_UNSUPPORTED, "fmt %d: 8 (Q8_0), 4 (Q4_0), 75 (Q4_K) or 1 (int8)", fmt);
     }
 }
 
@@ -297,6 +306,14 @@ hq_status hq_quantize_q4_0(const float *W, void *out, int64_t rows, int64_t cols
     if (rows < 1 || cols < 32 || cols % 32 != 0) return set_error(HQ_ERR_SHAPE, "need rows>=1, cols%%32==0");
     if (!aligned(W, 16) || !aligned(out, 2)) return set_error(HQ_ERR_ALIGN, "W must be 16-byte aligned");
     return finish(launch_quantize(1, W, out, nullptr, rows, cols, (cudaStream_t)stream));
+}
+
+hq_status hq_quantize_q4_k(const float *W, void *out, int64_t rows, int64_t cols, hq_stream_t stream) {
+    if (!W || !out) return set_error(HQ_ERR_NULL, "W and out must be non-null");
+    if (rows < 1 || cols < 256 || cols % 256 != 0) return set_error(HQ_ERR_SHAPE, "need rows>=1, cols%%256==0");
+    if (!aligned(W, 4) || !aligned(out, 16))
+        return set_error(HQ_ERR_ALIGN, "W must be 4-byte aligned and out 16-byte aligned");
+    return finish(launch_quantize(3, W, out, nullptr, rows, cols, (cudaStream_t)stream));
 }
 
 hq_status hq_quantize_i8_rows(const float *W, int8_t *Wq, float *scale, int64_t rows, int64_t cols,

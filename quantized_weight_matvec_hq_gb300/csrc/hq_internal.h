@@ -26,7 +26,7 @@ void *tensor_map_encoder();                         // PFN_cuTensorMapEncodeTile
 
 // QLoRA adapter epilogue of a float matvec: y += scale * B u, where u = A x
 // was computed by launch_lora_down earlier on the same stream.
-struct LoraArgs {
+struct MatvecExtras {
     const uint16_t *B = nullptr;    // bf16 [rows][rank]
     const float *u = nullptr;       // fp32 [n_vec][rank]
     float scale = 0.f;
@@ -35,9 +35,11 @@ struct LoraArgs {
 
 // Launchers (arguments already validated by the API layer).
 hq_status launch_matvec_float_q8_0(const void *W, const float *x, float *y, int64_t rows,
-                                   int64_t cols, int n_vec, const LoraArgs *lora, cudaStream_t stream);
+                                   int64_t cols, int n_vec, const MatvecExtras *lora, cudaStream_t stream);
 hq_status launch_matvec_float_q4_0(const void *W, const float *x, float *y, int64_t rows,
-                                   int64_t cols, int n_vec, const LoraArgs *lora, cudaStream_t stream);
+                                   int64_t cols, int n_vec, const MatvecExtras *lora, cudaStream_t stream);
+hq_status launch_matvec_float_q4_k(const void *W, const float *x, float *y, int64_t rows,
+                                   int64_t cols, int n_vec, const MatvecExtras *lora, cudaStream_t stream);
 hq_status launch_lora_down(const uint16_t *A, const float *x, float *u, int rank, int64_t cols,
                            int n_vec, cudaStream_t stream);
 // MoE epilogue of a grouped Q8_0 launch: 0 none; 1 SwiGLU over interleaved
@@ -62,6 +64,8 @@ hq_status launch_quantize(int fmt, const float *W, void *out, float *scale, int6
 hq_status debug_plan_float_q8_0(int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin, int regs,
                                 int64_t *out);
 hq_status debug_plan_float_q4_0(int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin, int regs,
+                                int64_t *out);
+hq_status debug_plan_float_q4_k(int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin, int regs,
                                 int64_t *out);
 hq_status debug_plan_i8(int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin, int regs, int64_t *out);
 

@@ -53,6 +53,8 @@
 #endif
 #if HQ_PART == 1
 #define HQ_PART_NAME(f) f##_q4_0
+#elif HQ_PART == 4
+#define HQ_PART_NAME(f) f##_q4_k
 #else
 #define HQ_PART_NAME(f) f##_q8_0
 #endif
@@ -84,6 +86,7 @@ struct PolQ8_0 {
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
     static constexpr bool kRowSplit = false;        // see PolRowSplit
+    static constexpr bool kNibbles = false;         // 4-bit quants (decode-bound launch policies)
     using Acc = float2;
     using Red = float;
 
@@ -226,6 +229,7 @@ struct PolQ4_0 {
     static constexpr int kConsWarpsFewAcc = 4;      // n_vec 1 (two rows per lane; see make_plan's ring)
     static constexpr bool kComputeBound = true;     // decode, not HBM, sets the pace
     static constexpr bool kRowSplit = false;
+    static constexpr bool kNibbles = true;
     using Acc = float2;
     using Red = float;
 
@@ -302,6 +306,122 @@ struct PolQ4_0 {
     __device__ __forceinline__ static Red finish(const Acc &a) { return a.x + a.y; }
 };
 
+// Q4_K ("One Native Stack ...", sections "The Unified Quant Core" and "Ported
+// Versus Novel": ggml's super-block of 256 weights in 144 B).  A 256-column
+// chunk of a row is exactly one super-block: 16-byte unit 0 holds fp16 d,
+// fp16 dmin and the 12 bytes of six-bit sub-block scales sc_j and mins m_j;
+// units 1..8 hold four groups of 32 quant bytes, sub-block 2g in the low
+// nibbles of group g and sub-block 2g+1 in the high nibbles; the weight is
+// w = d sc_j q - dmin m_j.
+//
+// Every weight is formed in fp32 before it multiplies x: the nibble is placed
+// in the mantissa of 2^23 (one lop3) and 2^23 removed exactly, leaving q 2^p;
+// then one packed fma gives (d sc_j 2^-p) (q 2^p) - dmin m_j = w, rounded once.
+// So the running sums hold partial sums of w x, and the rounding is bounded by
+// the products |w x| themselves, as for the symmetric formats.
+struct PolQ4_K {
+    static constexpr int kBlockBytes = 18;          // bytes per 32 columns (a super-block: 144 B per 256)
+    static constexpr int kChunkCols = 256;          // one super-block per row chunk
+    static constexpr int kChunkBytes = 144;         // = 9 x 16 B
+    static constexpr int kBoxInner = 36;            // uint32 words per chunk row
+    static constexpr int kXElemBytes = 4;
+    static constexpr int kUnits = 8;                // sub-blocks per chunk
+    static constexpr bool kSwizzle = false;
+    static constexpr int kConsWarps = 4;
+    static constexpr int kConsWarpsFewAcc = 4;
+    static constexpr bool kComputeBound = true;
+    static constexpr bool kRowSplit = false;
+    static constexpr bool kNibbles = true;
+    using Acc = float2;
+    using Red = float;
+
+    // six-bit scale (sel 0) or min (sel 1) of sub-block J from the header words
+    // s0 = bytes 4..7, s1 = bytes 8..11, s2 = bytes 12..15 of the super-block
+    template <int J, int SEL>
+    __device__ __forceinline__ static uint32_t six(uint32_t s0, uint32_t s1, uint32_t s2) {
+        if constexpr (J < 4) return ((SEL ? s1 : s0) >> (8 * J)) & 63u;
+        else {
+            const uint32_t lo4 = (s2 >> (8 * (J - 4) + 4 * SEL)) & 15u;
+            const uint32_t hi2 = ((SEL ? s1 : s0) >> (8 * (J - 4) + 6)) & 3u;
+            return lo4 | (hi2 << 4);
+        }
+    }
+
+    // sub-blocks [B0, B0 + 2): quant group B0 / 2 of every row the lane holds
+    template <int NV, int R, int B0, int NB>
+    __device__ __forceinline__ static void consume(const uint8_t *__restrict__ wt,
+                                                   const uint8_t *__restrict__ xt8, int lane,
+                                                   Acc (&acc)[R][NV]) {
+        static_assert(NB == 2 && B0 % 2 == 0, "one quant group per call");
+        constexpr int G = B0 / 2;
+        const float *xt = reinterpret_cast<const float *>(xt8);
+        const float2 kM = make_float2(-8388608.0f, -8388608.0f);          // -2^23
+        const uint32_t magic = opaque_magic();
+        float2 alo[R], ahi[R], blo[R], bhi[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint4 hdr = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes)[0];
+            const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
+            const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+            const float a0 = d * (float)six<B0, 0>(hdr.y, hdr.z, hdr.w);
+            const float a1 = d * (float)six<B0 + 1, 0>(hdr.y, hdr.z, hdr.w);
+            const float b0 = dm * (float)six<B0, 1>(hdr.y, hdr.z, hdr.w);
+            const float b1 = dm * (float)six<B0 + 1, 1>(hdr.y, hdr.z, hdr.w);
+            alo[r] = make_float2(a0, a0 * 0.00390625f);                  // nibbles at bits 0 and 8
+            ahi[r] = make_float2(a1 * 0.0625f, a1 * 0.000244140625f);     // nibbles at bits 4 and 12
+            blo[r] = make_float2(-b0, -b0);
+            bhi[r] = make_float2(-b1, -b1);
+        }
+        float2 shi[R][NV];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) shi[r][v] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {                   // the group's two 16-byte units
+            uint32_t qw[R][4];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint4 q = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes)[1 + 2 * G + u];
+                qw[r][0] = q.x; qw[r][1] = q.y; qw[r][2] = q.z; qw[r][3] = q.w;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {            // quant bytes 4k .. 4k+3 of the group
+                const int k = 4 * u + kk;
+                float4 xl[NV], xh[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    xl[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 64 * G + 4 * k);
+                    xh[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 64 * G + 32 + 4 * k);
+                }
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t w = h ? (qw[r][kk] >> 16) : qw[r][kk];
+                        const float2 qlo = fadd2(make_float2(nib<0xFu>(w, magic), nib<0xF00u>(w, magic)), kM);
+                        const float2 qhi = fadd2(make_float2(nib<0xF0u>(w, magic), nib<0xF000u>(w, magic)), kM);
+                        const float2 wlo = ffma2(alo[r], qlo, blo[r]);
+                        const float2 whi = ffma2(ahi[r], qhi, bhi[r]);
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) {
+                            const float2 xpl = h ? make_float2(xl[v].z, xl[v].w) : make_float2(xl[v].x, xl[v].y);
+                            const float2 xph = h ? make_float2(xh[v].z, xh[v].w) : make_float2(xh[v].x, xh[v].y);
+                            acc[r][v] = ffma2(wlo, xpl, acc[r][v]);
+                            shi[r][v] = ffma2(whi, xph, shi[r][v]);
+                        }
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) acc[r][v] = fadd2(acc[r][v], shi[r][v]);
+    }
+    __device__ __forceinline__ static Red finish(const Acc &a) { return a.x + a.y; }
+};
+
 struct PolI8 {
     static constexpr int kChunkCols = 128;          // one 128-byte swizzle span
     static constexpr int kChunkBytes = 128;
@@ -313,6 +433,7 @@ struct PolI8 {
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
     static constexpr bool kRowSplit = false;
+    static constexpr bool kNibbles = false;
     using Acc = int;
     using Red = int;
 
@@ -544,7 +665,8 @@ constexpr int ctas_per_sm() {
     // Q4_0 at 2-6 vectors: its 96-116 registers leave room for a third CTA
     // (8B-shaped token n_vec 3 / 4: 1865 / 1606 -> 1939 / 1651 GB/s; n_vec 2,
     // with a ring of one stage per warp: 2520 -> 2733 GB/s)
-    if constexpr (std::is_same<P, PolQ4_0>::value) if (NV >= 2 && NV <= 6) return 3;
+    // (Q4_K: up to 5; at 6 vectors its weights-then-products decode needs more)
+    if constexpr (P::kNibbles) if (NV >= 2 && NV <= (std::is_same<P, PolQ4_K>::value ? 5 : 6)) return 3;
     return cons_warps<P, NV, R>() >= 8 ? 2
          : cons_warps<P, NV, R>() >= 4 ? ((NV * R <= 2) ? 3 : 2)
                                         : ((NV * R <= 2) ? 5 : 3);
@@ -1106,8 +1228,8 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     // and so does the dense Q8_0 kernel at two vectors (PolQ8_0Two); the dense
     // Q8_0 kernel at one vector does not (8B token 5186 -> 4607 GB/s), nor the
     // MoE kernel at four vectors (2696 -> 2579 GB/s).
-    constexpr int kSpw = (((std::is_same<P, PolQ4_0>::value || std::is_same<P, PolQ8_0Moe>::value) && NV == 1) ||
-                          (std::is_same<P, PolQ4_0>::value && NV == 2) ||
+    constexpr int kSpw = (((P::kNibbles || std::is_same<P, PolQ8_0Moe>::value) && NV == 1) ||
+                          (P::kNibbles && NV == 2) ||
                           (std::is_same<P, PolQ8_0Two>::value && NV == 2)) ? 1 : 2;
     p.stages = kSpw * SQ;
     while (L::total(p.stages + SQ, 1) * want <= budget && p.stages < 4 * SQ) p.stages += SQ;
@@ -1268,12 +1390,12 @@ hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
 // x tile leaves room for too few CTAs per SM.
 template <class P>
 constexpr int rows_per_lane(int nv) {
-    return (std::is_same<P, PolQ4_0>::value && nv <= 2) ? 2 : 1;
+    return (P::kNibbles && nv <= 2) ? 2 : 1;
 }
 
 template <class P, int NV, int R>
 hq_status dense_nv_r(const DeviceInfo &dev, const void *W, const void *x, void *y, const int32_t *mult,
-                     const int32_t *shift, long long rows, long long cols, const LoraArgs *lora,
+                     const int32_t *shift, long long rows, long long cols, const MatvecExtras *lora,
                      cudaStream_t stream) {
     constexpr bool kI8 = std::is_same<P, PolI8>::value;
     constexpr int TR = Layout<P, NV, R, false>::TR;             // rows per tile (one TMA box)
@@ -1342,7 +1464,7 @@ hq_status with_dense_policy(long long cols, F &&f) {
 
 template <class P, int NV>
 hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y, const int32_t *mult,
-                   const int32_t *shift, long long rows, long long cols, const LoraArgs *lora,
+                   const int32_t *shift, long long rows, long long cols, const MatvecExtras *lora,
                    cudaStream_t stream) {
     return with_dense_policy<P, NV>(cols, [&](auto pol, auto rt) {
         return dense_nv_r<decltype(pol), NV, decltype(rt)::value>(dev, W, x, y, mult, shift, rows, cols, lora,
@@ -1401,7 +1523,7 @@ hq_status plan_dispatch(const DeviceInfo &dev, long long rows, long long cols, i
 template <class P>
 hq_status dense_dispatch(const DeviceInfo &dev, const void *W, const void *x, void *y,
                          const int32_t *mult, const int32_t *shift, long long rows, long long cols,
-                         int n_vec, const LoraArgs *lora, cudaStream_t stream) {
+                         int n_vec, const MatvecExtras *lora, cudaStream_t stream) {
     switch (n_vec) {
         case 1: return dense_nv<P, 1>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
         case 2: return dense_nv<P, 2>(dev, W, x, y, mult, shift, rows, cols, lora, stream);
@@ -1467,21 +1589,25 @@ hq_status moe_nv(const DeviceInfo &dev, const void *W_bank, const int32_t *ids, 
 
 }  // namespace
 
-// The public launchers are compiled in four parts (HQ_PART 0..3, one object
+// The public launchers are compiled in five parts (HQ_PART 0..4, one object
 // file each) so that the template instantiations build in parallel.
-#if !defined(HQ_PART) || HQ_PART == 0 || HQ_PART == 1
+#if !defined(HQ_PART) || HQ_PART == 0 || HQ_PART == 1 || HQ_PART == 4
+// the float format of this part: Q8_0 (part 0), Q4_0 (part 1), Q4_K (part 4)
+using PartPol = std::conditional<HQ_PART == 1, PolQ4_0, std::conditional<HQ_PART == 4, PolQ4_K, PolQ8_0>::type>::type;
+
 hq_status HQ_PART_NAME(launch_matvec_float)(const void *W, const float *x, float *y, int64_t rows,
-                                            int64_t cols, int n_vec, const LoraArgs *lora,
+                                            int64_t cols, int n_vec, const MatvecExtras *lora,
                                             cudaStream_t stream) {
     constexpr int FMT = (HQ_PART == 1) ? 1 : 0;
-    using P = std::conditional<FMT == 0, PolQ8_0, PolQ4_0>::type;
+    using P = PartPol;
     DeviceInfo *dev = nullptr;
     hq_status st = device_info(&dev);
     if (st != HQ_OK) return st;
     if (cols % 256 == 0) return dense_dispatch<P>(*dev, W, x, y, nullptr, nullptr, rows, cols, n_vec, lora, stream);
+    if (HQ_PART == 4) return set_error(HQ_ERR_SHAPE, "Q4_K needs cols %% 256 == 0 (cols = %lld)", (long long)cols);
     const unsigned grid = (unsigned)((rows + 7) / 8);
-    const LoraArgs none;
-    const LoraArgs &l = lora ? *lora : none;
+    const MatvecExtras none;
+    const MatvecExtras &l = lora ? *lora : none;
     note_launch();
     matvec_plain_kernel<FMT><<<grid, 256, 0, stream>>>((const uint8_t *)W, x, y, rows, cols, n_vec,
                                                        l.B, l.u, l.scale, l.rank);
@@ -1491,10 +1617,10 @@ hq_status HQ_PART_NAME(launch_matvec_float)(const void *W, const float *x, float
 }
 #endif
 
-#if !defined(HQ_PART) || HQ_PART == 0 || HQ_PART == 1
+#if !defined(HQ_PART) || HQ_PART == 0 || HQ_PART == 1 || HQ_PART == 4
 hq_status HQ_PART_NAME(debug_plan_float)(int n_vec, int64_t rows, int64_t cols, int num_sms, int smem_optin,
                                          int regs, int64_t *out) {
-    using P = std::conditional<HQ_PART == 1, PolQ4_0, PolQ8_0>::type;
+    using P = PartPol;
     DeviceInfo dev;
     dev.num_sms = num_sms;
     dev.max_smem_optin = smem_optin;

@@ -7,6 +7,11 @@
 // zen-nano (Qwen3-0.6B) to deterministic on-chain inference", section
 // "Quantization recipe (validated)" (s_w[o] = max|W[o,:]|/127, round(W/s_w)).
 //
+// Q4_K: the same page's section "Ported Versus Novel" (every format taken
+// verbatim from ggml): a super-block of 256 weights in 144 B = fp16 d, fp16
+// dmin, 12 B of six-bit sub-block scales and mins, 128 B of nibbles; encoded
+// with a plain min/max reading (the pages give no encoder).
+//
 // Every decision that turns a float into an integer code is taken in IEEE
 // fp32 with correctly rounded division (no fast-math), so the bytes are the
 // same on any conforming implementation of the same reading.
@@ -80,6 +85,72 @@ quantize_q4_0_kernel(const float *__restrict__ W, uint8_t *__restrict__ out, lon
         blk[1 + j / 2] = (unsigned short)((n[j] | (n[j + 16] << 4)) | ((n[j + 1] | (n[j + 17] << 4)) << 8));
 }
 
+// One thread per Q4_K super-block.  Per 32-weight sub-block j: mn = min(0,
+// min w), mx = max w, scale_j = (mx - mn)/15, min_j = -mn; d = (largest
+// scale)/63 and dmin = (largest min)/63 stored fp16; sc_j = round(scale_j *
+// 63/largest scale), m_j likewise, both at most 63; then with a = d sc_j and b
+// = dmin m_j from the stored fp16 values, q = round((w + b)/a) clamped to
+// [0, 15] (0 when a is 0).  Packing: bytes 4..15 carry the six-bit fields (see
+// the header), bytes 16..143 hold four groups of 32 bytes, sub-block 2g in the
+// low nibbles of group g and sub-block 2g+1 in the high nibbles.
+__global__ void __launch_bounds__(128)
+quantize_q4_k_kernel(const float *__restrict__ W, uint8_t *__restrict__ out, long long n_sb) {
+    const long long b = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= n_sb) return;
+    const float *w = W + b * 256;
+    float scale[8], minv[8], max_scale = 0.f, max_min = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float mn = w[32 * j], mx = w[32 * j];
+        for (int l = 1; l < 32; ++l) {
+            const float v = w[32 * j + l];
+            if (v < mn) mn = v;
+            if (v > mx) mx = v;
+        }
+        if (mn > 0.f) mn = 0.f;
+        scale[j] = __fdiv_rn(__fsub_rn(mx, mn), 15.0f);
+        minv[j] = -mn;
+        if (scale[j] > max_scale) max_scale = scale[j];
+        if (minv[j] > max_min) max_min = minv[j];
+    }
+    const unsigned short dh = __half_as_ushort(__float2half_rn(__fdiv_rn(max_scale, 63.0f)));
+    const unsigned short mh = __half_as_ushort(__float2half_rn(__fdiv_rn(max_min, 63.0f)));
+    const float inv_s = max_scale > 0.f ? __fdiv_rn(63.0f, max_scale) : 0.f;
+    const float inv_m = max_min > 0.f ? __fdiv_rn(63.0f, max_min) : 0.f;
+    int sc[8], mq[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        sc[j] = max(0, min(63, (int)roundf(__fmul_rn(scale[j], inv_s))));
+        mq[j] = max(0, min(63, (int)roundf(__fmul_rn(minv[j], inv_m))));
+    }
+    uint32_t s12[3] = {0u, 0u, 0u};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        s12[0] |= (uint32_t)(sc[j] | ((sc[j + 4] >> 4) << 6)) << (8 * j);
+        s12[1] |= (uint32_t)(mq[j] | ((mq[j + 4] >> 4) << 6)) << (8 * j);
+        s12[2] |= (uint32_t)((sc[j + 4] & 15) | ((mq[j + 4] & 15) << 4)) << (8 * j);
+    }
+    uint4 *blk = reinterpret_cast<uint4 *>(out + b * 144);     // 144 = 9 x 16 B
+    blk[0] = make_uint4((uint32_t)dh | ((uint32_t)mh << 16), s12[0], s12[1], s12[2]);
+    const float dq = __half2float(__ushort_as_half(dh)), mqf = __half2float(__ushort_as_half(mh));
+    uint32_t *qs = reinterpret_cast<uint32_t *>(out + b * 144 + 16);
+    for (int g = 0; g < 4; ++g) {
+        const float a0 = __fmul_rn(dq, (float)sc[2 * g]), b0 = __fmul_rn(mqf, (float)mq[2 * g]);
+        const float a1 = __fmul_rn(dq, (float)sc[2 * g + 1]), b1 = __fmul_rn(mqf, (float)mq[2 * g + 1]);
+        for (int l = 0; l < 32; l += 4) {
+            uint32_t word = 0u;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                int lo = 0, hi = 0;
+                if (a0 > 0.f) lo = max(0, min(15, (int)roundf(__fdiv_rn(__fadd_rn(w[64 * g + l + i], b0), a0))));
+                if (a1 > 0.f) hi = max(0, min(15, (int)roundf(__fdiv_rn(__fadd_rn(w[64 * g + 32 + l + i], b1), a1))));
+                word |= (uint32_t)(lo | (hi << 4)) << (8 * i);
+            }
+            qs[8 * g + l / 4] = word;
+        }
+    }
+}
+
 // One CTA per row: scale = max|w|/127, q = round(w/scale) in [-127, 127].
 __global__ void __launch_bounds__(256)
 quantize_i8_rows_kernel(const float *__restrict__ W, int8_t *__restrict__ Wq, float *__restrict__ scale,
@@ -108,6 +179,10 @@ hq_status launch_quantize(int fmt, const float *W, void *out, float *scale, int6
     if (fmt == 2) {
         note_launch();
         quantize_i8_rows_kernel<<<(unsigned)rows, 256, 0, stream>>>(W, (int8_t *)out, scale, cols);
+    } else if (fmt == 3) {
+        const long long nsb = rows * (cols / 256);
+        note_launch();
+        quantize_q4_k_kernel<<<(unsigned)((nsb + 127) / 128), 128, 0, stream>>>(W, (uint8_t *)out, nsb);
     } else {
         const long long nb = rows * (cols / 32);
         const unsigned grid = (unsigned)((nb + 255) / 256);

@@ -73,6 +73,13 @@ def test_host_validation_before_any_launch(hq):
     assert L.hq_moe_matvec_q8_0_combine(fake, fake, fake, 1, 0, fake, 4, 2, 8, 256, 1, 0) == hq.HQ_ERR_NULL
     assert L.hq_moe_matvec_q8_0_combine(fake, fake, fake, 1, fake + 2, fake, 4, 2, 8, 256, 1, 0) == hq.HQ_ERR_ALIGN
     assert L.hq_moe_matvec_q8_0_combine(fake, fake, fake, 1, fake, fake, 4, 5, 8, 256, 1, 0) == hq.HQ_ERR_SHAPE
+    # Q4_K: super-blocks of 256 columns, W and x 16-byte aligned
+    assert L.hq_matvec_q4_k(fake, fake, fake, 4, 288, 1, 0) == hq.HQ_ERR_SHAPE
+    assert L.hq_matvec_q4_k(fake, fake, fake, 4, 224, 1, 0) == hq.HQ_ERR_SHAPE
+    assert L.hq_matvec_q4_k(fake + 8, fake, fake, 4, 256, 1, 0) == hq.HQ_ERR_ALIGN
+    assert L.hq_matvec_q4_k(fake, fake, fake, 4, 256, 0, 0) == hq.HQ_ERR_NVEC
+    assert L.hq_quantize_q4_k(fake, fake, 4, 288, 0) == hq.HQ_ERR_SHAPE
+    assert L.hq_quantize_q4_k(fake, fake + 8, 4, 256, 0) == hq.HQ_ERR_ALIGN
     # quantizers
     assert L.hq_quantize_q8_0(fake, fake, 4, 40, 0) == hq.HQ_ERR_SHAPE
     assert L.hq_quantize_q4_0(0, fake, 4, 64, 0) == hq.HQ_ERR_NULL
@@ -108,7 +115,8 @@ def test_requant_params_match_oracle(hq):
 
 def test_header_cites_each_entry_point():
     text = open(os.path.join(ROOT, "include", "hq.h")).read()
-    for name in ("hq_matvec_q8_0", "hq_matvec_q4_0", "hq_matvec_i8_requant", "hq_moe_matvec_q8_0",
-                 "hq_quantize_q8_0", "hq_requant_params", "hq_requant_i32_debug"):
+    for name in ("hq_matvec_q8_0", "hq_matvec_q4_0", "hq_matvec_q4_k", "hq_matvec_i8_requant",
+                 "hq_moe_matvec_q8_0", "hq_quantize_q8_0", "hq_quantize_q4_k", "hq_requant_params",
+                 "hq_requant_i32_debug"):
         block = text[text.index(" * " + name) if (" * " + name) in text else text.index(name):]
         assert "Source:" in block.split(");")[0] or "Source:" in block[:2500], name

@@ -21,6 +21,7 @@ def total_weight_bytes(ops):
     ("8b-q8_0-unfused", 225, 7_973_699_584),
     ("8b-q4_0", 129, 4_221_370_368),
     ("8b-q4_0-unfused", 225, 4_221_370_368),
+    ("8b-q4_k", 129, 4_221_370_368),
     ("qwen3-0.6b-q8_0", 113, 633_233_408),
     ("qwen3-0.6b-q8_0-unfused", 197, 633_233_408),
 ])
