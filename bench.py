@@ -556,6 +556,7 @@ class OracleSample:
                 distinct.append(op)
         g = synthetic.rng(seed)
         self.calls = []
+        self.dense = []                            # (blocks, x, rows, cols) of the plain dense calls
         self.pass_bytes = 0
         for op in distinct:
             if op.kind == "dense":
@@ -564,6 +565,8 @@ class OracleSample:
                 blocks = oracle.quantize(self.fmt, W)
                 x = synthetic.activations(g, n_vec, op.cols)
                 self.calls.append(lambda b=blocks, x=x, r=r, c=op.cols: oracle.matvec(self.fmt, b, x, r, c))
+                if not op.lora_rank:
+                    self.dense.append((blocks, x, r, op.cols))
                 self.pass_bytes += weight_bytes(self.fmt, r, op.cols)
                 if op.lora_rank:
                     # the adapter term of the same sampled rows (bf16 bit patterns of N(0, 0.02))
@@ -620,6 +623,88 @@ class OracleSample:
             if el >= budget_s:
                 return done / el / 1e9, self.describe(n), el
 
+    def timed_all_cores(self, budget_s, workers):
+        """The same dense sample with each call's rows split over `workers`
+        host threads (the C oracle runs with the interpreter lock released, so
+        the threads run on separate cores).  None for non-dense workloads."""
+        if self.kind != "dense" or not self.dense:
+            return None
+        import concurrent.futures as cf
+        oracle = self.oracle
+        jobs = []
+        for (blocks, x, r, c) in self.dense:
+            bounds = np.linspace(0, r, workers + 1).astype(int)
+            jobs += [(blocks, x, r, c, int(lo), int(hi)) for lo, hi in zip(bounds[:-1], bounds[1:]) if hi > lo]
+        per_pass = sum(weight_bytes(self.fmt, r, c) for (_, _, r, c) in self.dense)
+        done, n, t0 = 0, 0, time.perf_counter()
+        with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+            while True:
+                list(ex.map(lambda j: oracle.matvec_rows(self.fmt, j[0], j[1], j[2], j[3], j[4], j[5]), jobs))
+                done += per_pass
+                n += 1
+                el = time.perf_counter() - t0
+                if el >= budget_s:
+                    desc = (f"{n} passes; each = the first rows (~4M weights) of each of the {len(self.dense)} "
+                            f"distinct {self.model} matrix shapes, {per_pass / 1e6:.1f} MB of {self.fmt} weights, "
+                            f"n_vec={self.n_vec}, every call's rows split over {workers} threads of the C oracle "
+                            f"(f64 accumulation)")
+                    return done / el / 1e9, desc, el
+
+
+# ----------------------------------------------------------------- sweep
+
+# the north-star metric's other points, measured in the default run: the same
+# 8B decode token at the speculative-verify widths, and in the 4-bit formats
+SWEEP = [("8b-q8_0", 2), ("8b-q8_0", 4), ("8b-q8_0", 8), ("8b-q4_0", 1), ("8b-q4_k", 1)]
+
+
+def roof_of(ops, n_vec, dev_ms, alg_total, peak, sm_mhz, n_sms):
+    """Roofline of a step: HBM (bytes against the measured copy bandwidth)
+    unless its flops per byte exceed the FP32 ridge, then the FP32 pipe."""
+    achieved = alg_total / (dev_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4)}
+    flops = fp32_flops(ops, n_vec)
+    if flops is not None and sm_mhz:
+        fp32_peak = n_sms * 128 * 2 * sm_mhz * 1e6 / 1e12
+        if flops / alg_total > fp32_peak * 1e3 / peak:
+            tflops = flops / (dev_ms / 1e3) / 1e12
+            roof = {"bound": "alu", "achieved": round(tflops, 2), "peak": round(fp32_peak, 1), "unit": "TFLOP/s",
+                    "frac": round(tflops / fp32_peak, 4),
+                    "peak_basis": f"{n_sms} SMs x 128 FP32 FMA/clk x 2 x {sm_mhz} MHz"}
+    return roof
+
+
+def sweep_entry(workload, n_vec, steps, warmup, device, peak, seed):
+    """One point of the sweep: the step's graph replayed `steps` times after
+    `warmup`, CUDA events on the replay stream, clocks sampled meanwhile."""
+    import torch
+    step = Step(workload, n_vec, device, seed)
+    graph = step.capture()
+    for _ in range(warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(device.index or 0) as clocks:
+        e0.record()
+        for _ in range(steps):
+            graph.replay()
+        e1.record()
+        e1.synchronize()
+    dev_ms = e0.elapsed_time(e1) / steps
+    clk = clocks.summary()
+    n_sms = torch.cuda.get_device_properties(device).multi_processor_count
+    alg = float(sum(step.alg_bytes))
+    out = {"workload": workload, "format": step.fmt, "n_vec": n_vec,
+           "value": round(step.weight_bytes / (dev_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+           "ms_per_step": round(dev_ms, 5), "tok_per_s": round(1e3 / dev_ms * n_vec, 2),
+           "roofline": roof_of(step.ops, n_vec, dev_ms, alg, peak, clk.get("sm_mhz"), n_sms),
+           "clocks": clk}
+    del graph, step
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
 
 # ----------------------------------------------------------------- main
 
@@ -657,6 +742,8 @@ def main():
     ap.add_argument("--format", choices=["q8_0", "q4_0", "q4_k"], default="q8_0", help="format for --shape")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle time for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the sweep over n_vec and formats that the default 8B Q8_0 run adds")
     ap.add_argument("--traffic-file", default=os.path.join(ROOT, "profiles", "dram_traffic.txt"),
                     help="DRAM bytes per step of the matvec kernel, from an ncu capture (text)")
     args = ap.parse_args()
@@ -838,10 +925,26 @@ def main():
     if fmt in ("q4_0", "q4_k") and args.n_vec <= 2:
         line["roofline"]["limiter"] = ("nibble decode issue rate (one and per weight on the ALU pipe, one ffma2 "
                                        "per two weights on the FMA pipe), not HBM")
+    # the rest of the benchmark spec's metric (n_vec 2, 4, 8; Q4_0 and Q4_K at one
+    # vector), one GPU, after the headline's buffers are released
+    if (world == 1 and not args.no_sweep and not args.shape and args.workload == "8b-q8_0"
+            and args.n_vec == 1):
+        del graph, graph_ev, step
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["sweep"] = [sweep_entry(w, nv, args.steps, args.warmup, device, peak, synthetic.SEED_BASE + 2)
+                         for (w, nv) in SWEEP]
     if not args.no_cpu_baseline and not args.shape:
-        gbs, desc, el = OracleSample(args.workload, args.n_vec).timed(args.cpu_budget)
+        samp = OracleSample(args.workload, args.n_vec)
+        gbs, desc, el = samp.timed(args.cpu_budget)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": desc, "seconds": round(el, 2), "cpu": cpu_model()}
+        workers = os.cpu_count() or 1
+        par = samp.timed_all_cores(args.cpu_budget / 2, workers)
+        if par is not None:
+            line["cpu_baseline_all_cores"] = {"value": round(par[0], 4), "unit": "GB/s", "cores": workers,
+                                              "kind": "oracle", "sample": par[1], "seconds": round(par[2], 2),
+                                              "cpu": cpu_model()}
     print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
