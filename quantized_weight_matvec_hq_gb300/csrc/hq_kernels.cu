@@ -86,6 +86,7 @@ struct PolQ8_0 {
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
     static constexpr bool kRowSplit = false;        // see PolRowSplit
+    static constexpr bool kColSplit = false;        // see PolColSplit
     static constexpr bool kNibbles = false;         // 4-bit quants (decode-bound launch policies)
     using Acc = float2;
     using Red = float;
@@ -229,6 +230,7 @@ struct PolQ4_0 {
     static constexpr int kConsWarpsFewAcc = 4;      // n_vec 1 (two rows per lane; see make_plan's ring)
     static constexpr bool kComputeBound = true;     // decode, not HBM, sets the pace
     static constexpr bool kRowSplit = false;
+    static constexpr bool kColSplit = false;
     static constexpr bool kNibbles = true;
     using Acc = float2;
     using Red = float;
@@ -331,6 +333,7 @@ struct PolQ4_K {
     static constexpr int kConsWarpsFewAcc = 4;
     static constexpr bool kComputeBound = true;
     static constexpr bool kRowSplit = false;
+    static constexpr bool kColSplit = false;
     static constexpr bool kNibbles = true;
     using Acc = float2;
     using Red = float;
@@ -433,6 +436,7 @@ struct PolI8 {
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
     static constexpr bool kRowSplit = false;
+    static constexpr bool kColSplit = false;
     static constexpr bool kNibbles = false;
     using Acc = int;
     using Red = int;
@@ -475,6 +479,17 @@ struct PolI8 {
 template <class Base>
 struct PolRowSplit : Base {
     static constexpr bool kRowSplit = true;
+};
+
+// Column-split stages (the 4-bit formats at one vector, whose decode sets the
+// pace).  As with row-split stages every consumer warp consumes every stage,
+// but each takes its own blocks of all the stage's rows; the tile's partial
+// sums are added across the warps at its end.  A stage is then in use for a
+// quarter of the time one warp would need for it, so the same shared memory
+// keeps more bytes in flight.
+template <class Base>
+struct PolColSplit : Base {
+    static constexpr bool kColSplit = true;
 };
 
 template <class Acc> __device__ __forceinline__ Acc zero_acc();
@@ -633,6 +648,19 @@ __device__ __forceinline__ void consume_chunk(const uint8_t *wt, const uint8_t *
     P::template consume<NV, R, 6, 2>(wt, xt, lane, acc);
 }
 
+// Column split: warp w of four consumes units [2w, 2w + 2) of every stage.
+template <class P, int NV, int R>
+__device__ __forceinline__ void consume_cols(const uint8_t *wt, const uint8_t *xt, int lane, int warp,
+                                             typename P::Acc (&acc)[R][NV]) {
+    static_assert(cons_warps<P, NV, R>() == 4 && P::kUnits == 8, "four warps of two units each");
+    switch (warp) {
+        case 0: P::template consume<NV, R, 0, 2>(wt, xt, lane, acc); break;
+        case 1: P::template consume<NV, R, 2, 2>(wt, xt, lane, acc); break;
+        case 2: P::template consume<NV, R, 4, 2>(wt, xt, lane, acc); break;
+        default: P::template consume<NV, R, 6, 2>(wt, xt, lane, acc); break;
+    }
+}
+
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -700,11 +728,12 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
     const int nthreads = blockDim.x;
     constexpr int CW = cons_warps<P, NV, R>();      // S % CW == 0 unless rows are split (see make_plan)
     constexpr bool RS = P::kRowSplit;
+    constexpr bool SH = P::kRowSplit || P::kColSplit;   // every warp consumes every stage
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
-            mbar_init(smem_u32(&empty[i]), P::kRowSplit ? CW : 1);   // row split: every warp frees the stage
+            mbar_init(smem_u32(&empty[i]), SH ? CW : 1);   // row / column split: every warp frees the stage
         }
         mbar_init(smem_u32(gather_bar), (uint32_t)max(a.ksplit - 1, 1));
         *abort_flag = 0;
@@ -858,13 +887,14 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
             // so a wait can never mistake a stage's previous phase for its next.
             // Row split: every warp consumes every fill (its own 32 * R rows of
             // the stage), so each warp waits on every phase of every stage in order.
-            for (int j = RS ? 0 : (warp - (int)(base % CW) + CW) % CW; j < nloc; j += RS ? 1 : CW) {
+            for (int j = SH ? 0 : (warp - (int)(base % CW) + CW) % CW; j < nloc; j += SH ? 1 : CW) {
                 const uint32_t n = base + j;
                 const int s = n % S;
                 mbar_wait(smem_u32(&full[s]), (n / S) & 1, abort_flag, a.fault);
                 uint8_t *st = smem + (size_t)s * ST;
                 if constexpr (!MOE) {
-                    consume_chunk<P, NV, R>(st + (RS ? (size_t)warp * 32 * R * P::kChunkBytes : 0), st + WT, lane, acc);
+                    if constexpr (P::kColSplit) consume_cols<P, NV, R>(st, st + WT, lane, warp, acc);
+                    else consume_chunk<P, NV, R>(st + (RS ? (size_t)warp * 32 * R * P::kChunkBytes : 0), st + WT, lane, acc);
                 } else {
                     // only the group's m vectors are multiplied
                     switch (m) {
@@ -1216,7 +1246,8 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     constexpr int CW = cons_warps<P, NV, R>();
     // stages come in multiples of CW (one owner each), or of one when every warp
     // consumes every stage (row split)
-    constexpr int SQ = P::kRowSplit ? 1 : CW;
+    constexpr bool SH = P::kRowSplit || P::kColSplit;
+    constexpr int SQ = SH ? 1 : CW;
     // two stages per consumer warp (a double buffer each), more when room allows;
     // row split: two stages for the CTA, more when room allows
     // Q4_0 at one vector starts from one stage per warp: with four consumer
@@ -1231,7 +1262,7 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     constexpr int kSpw = (((P::kNibbles || std::is_same<P, PolQ8_0Moe>::value) && NV == 1) ||
                           (P::kNibbles && NV == 2) ||
                           (std::is_same<P, PolQ8_0Two>::value && NV == 2)) ? 1 : 2;
-    p.stages = kSpw * SQ;
+    p.stages = SH ? 2 : kSpw * SQ;
     while (L::total(p.stages + SQ, 1) * want <= budget && p.stages < 4 * SQ) p.stages += SQ;
     p.smem = L::total(p.stages, 1);
     const int regs = std::max(32, regs_per_thread);
@@ -1264,7 +1295,7 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     // per SM get deeper rings, so an SM keeps about the same bytes in flight
     const long long resident = std::min<long long>(per_sm, std::max<long long>(1, (p.grid + dev.num_sms - 1) / dev.num_sms));
     int st = p.stages;
-    const int st_min = P::kRowSplit ? 2 : CW;
+    const int st_min = SH ? 2 : CW;
     while (st > st_min && L::total(st, lks) * resident > budget) st -= SQ;    // room for the gather buffer
     while (st + SQ <= 16 && L::total(st + SQ, lks) * resident <= budget) st += SQ;
     {
@@ -1274,7 +1305,7 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
         // (a group split's items are data-dependent: it keeps the full ring)
         const long long items = (ks > 1) ? 1 : gsplit >= 1 ? 1LL << 30 : (n_work + p.grid - 1) / std::max(p.grid, 1);
         const long long fills = items * ((n_chunks + ks - 1) / ks);
-        const long long need = P::kRowSplit ? std::max<long long>(2, fills)
+        const long long need = SH ? std::max<long long>(2, fills)
                                             : std::max<long long>(CW, (fills + CW - 1) / CW * CW);
         if (need < st) st = (int)need;
     }
@@ -1442,7 +1473,7 @@ hq_status dense_nv_r(const DeviceInfo &dev, const void *W, const void *x, void *
 // and R as an integral_constant; the launch and the test-only plan query
 // (hq_debug_plan) both go through here, so they cannot disagree.
 template <class P, int NV, class F>
-hq_status with_dense_policy(long long cols, F &&f) {
+hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long cols, F &&f) {
     constexpr int R = rows_per_lane<P>(NV);
     using RT = std::integral_constant<int, R>;
     if constexpr (std::is_same<P, PolQ8_0>::value && NV == 1) {
@@ -1457,6 +1488,15 @@ hq_status with_dense_policy(long long cols, F &&f) {
         // owner per stage: with its 128-row split stages it measured 1866 / 1605 /
         // 1007 -> 1794 / 1586 / 926 GB/s at n_vec 3 / 4 / 8.
         return f(PolRowSplit<P>{}, RT{});
+    } else if constexpr (P::kNibbles && NV == 1) {
+        // column-split stages where the launch does not split K over clusters
+        // (enough 64-row tiles to give every CTA slot two): Q4_0 gate|up
+        // 28672x4096 3386 -> 3635 GB/s; with a K split they lost (o 4096x4096
+        // 1622 -> 1482, down 4096x14336 2877 -> 2413 GB/s)
+        constexpr int TR = 32 * R;
+        const bool k_split = (rows + TR - 1) / TR * 2 <= (long long)dev.num_sms * ctas_per_sm<P, NV, R>();
+        if (!k_split) return f(PolColSplit<P>{}, RT{});
+        return f(P{}, RT{});
     } else {
         return f(P{}, RT{});
     }
@@ -1466,7 +1506,7 @@ template <class P, int NV>
 hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y, const int32_t *mult,
                    const int32_t *shift, long long rows, long long cols, const MatvecExtras *lora,
                    cudaStream_t stream) {
-    return with_dense_policy<P, NV>(cols, [&](auto pol, auto rt) {
+    return with_dense_policy<P, NV>(dev, rows, cols, [&](auto pol, auto rt) {
         return dense_nv_r<decltype(pol), NV, decltype(rt)::value>(dev, W, x, y, mult, shift, rows, cols, lora,
                                                                    stream);
     });
@@ -1477,7 +1517,7 @@ template <class Pol>
 constexpr int policy_id() {
     return std::is_same<Pol, PolQ8_0Short>::value ? 1
          : std::is_same<Pol, PolQ8_0Two>::value ? 2
-         : Pol::kRowSplit ? 3 : 0;
+         : Pol::kRowSplit ? 3 : Pol::kColSplit ? 4 : 0;
 }
 
 // Test-only: the geometry make_plan gives one dense launch, for a device
@@ -1485,7 +1525,7 @@ constexpr int policy_id() {
 // of `regs` registers per thread.
 template <class P, int NV>
 hq_status dense_plan(const DeviceInfo &dev, long long rows, long long cols, int regs, int64_t *out) {
-    return with_dense_policy<P, NV>(cols, [&](auto pol, auto rt) {
+    return with_dense_policy<P, NV>(dev, rows, cols, [&](auto pol, auto rt) {
         using Pol = decltype(pol);
         constexpr int R = decltype(rt)::value;
         using L = Layout<Pol, NV, R, false>;

@@ -456,14 +456,23 @@ def test_q8_0_launch_policy_boundaries(hq, rows, cols, n_vec):
     assert_within(y, y_ref, T, f"q8_0 {rows}x{cols} n_vec={n_vec}")
 
 
-@pytest.mark.parametrize("rows,cols,n_vec", [(4100, 4096, 1), (333, 14336, 1), (4100, 4096, 5)])
-def test_q4_0_launch_policy_boundaries(hq, rows, cols, n_vec):
-    """Q4_0 at one vector (four consumer warps, a ring of one stage per warp)
-    and at five vectors (three CTAs per SM), ragged last tiles, against the
-    oracle."""
+@pytest.mark.parametrize("fmt,rows,cols,n_vec", [
+    ("q4_0", 4100, 4096, 1), ("q4_0", 333, 14336, 1), ("q4_0", 4100, 4096, 5),
+    # one vector: K split over clusters up to 228 tiles of 64 rows on 152 SMs,
+    # column-split stages from 229 tiles on (ragged last tiles both sides)
+    ("q4_0", 14592, 512, 1), ("q4_0", 14593, 512, 1), ("q4_0", 20000, 768, 1),
+    ("q4_k", 14592, 512, 1), ("q4_k", 14593, 512, 1)])
+def test_nibble_launch_policy_boundaries(hq, fmt, rows, cols, n_vec):
+    """Q4_0 / Q4_K at one vector (four consumer warps: one stage per warp with a
+    K split, column-split stages without) and at five vectors (three CTAs per
+    SM), ragged last tiles, against the oracle."""
     g = synthetic.rng(5151 + rows + cols + n_vec)
-    blocks = quant("q4_0", synthetic.weights(g, rows, cols))
+    blocks = oracle.quantize(fmt, synthetic.weights(g, rows, cols))
     x = synthetic.activations(g, n_vec, cols)
-    y_ref, T = oracle.matvec("q4_0", blocks, x, rows, cols)
-    y = gpu_matvec(hq, "q4_0", blocks, x, rows, cols)
-    assert_within(y, y_ref, T, f"q4_0 {rows}x{cols} n_vec={n_vec}")
+    y_ref, T = oracle.matvec(fmt, blocks, x, rows, cols)
+    n = x.shape[0]
+    y = torch.full((n, rows), float("nan"), dtype=torch.float32, device="cuda")
+    fn = {"q4_0": hq.hq_matvec_q4_0, "q4_k": hq.hq_matvec_q4_k}[fmt]
+    fn(dev(blocks), dev(x), y, rows, cols, n)
+    torch.cuda.synchronize()
+    assert_within(y.cpu().numpy(), y_ref, T, f"{fmt} {rows}x{cols} n_vec={n_vec}")

@@ -49,7 +49,9 @@ PINS = [
     ((8, 1, 1024, 3072, 78), (256, 160, 8, None)),       # Qwen3-0.6B down
     ((8, 1, 151936, 1024, 78), (297, 160, 1, None)),     # Qwen3-0.6B lm_head
     ((8, 4, 28672, 4096, 98), (448, 96, 1, 65744)),      # row-split stages, n_vec 4 (full capture)
-    ((4, 1, 28672, 4096, 97), (448, 160, 1, 42208)),     # Q4_0 gate|up (full capture)
+    ((4, 1, 28672, 4096, 88), (448, 160, 1, 72976)),     # Q4_0 gate|up, column-split stages (full capture)
+    ((75, 1, 28672, 4096, 121), (448, 160, 1, 72976)),   # Q4_K gate|up, column-split stages (full capture)
+    ((8, 1, 4096, 4096, 80), (512, 96, 4, 39904)),       # Q8_0 o (full capture)
     ((4, 1, 4096, 14336, 97), (256, 160, 4, None)),
     ((4, 1, 6144, 4096, 97), (384, 160, 4, None)),
     ((4, 1, 4096, 4096, 97), (256, 160, 4, None)),
@@ -68,13 +70,17 @@ def test_plan_matches_the_recorded_launches(hq, args, want):
         assert p["smem"] == smem
 
 
-def expected_policy(fmt, n_vec, cols):
+def expected_policy(fmt, n_vec, rows, cols):
     if fmt == 8 and n_vec == 1:
         return 1 if cols <= 3072 else 0
     if fmt == 8 and n_vec == 2:
         return 2
     if fmt == 8:
         return 3
+    if fmt in (4, 75) and n_vec == 1:
+        # column-split stages unless K is split over clusters (64-row tiles too
+        # few to give each of the 152 x 3 CTA slots two)
+        return 4 if math.ceil(rows / 64) * 2 > GB300["num_sms"] * 3 else 0
     return 0
 
 
@@ -82,7 +88,7 @@ ROWS = [1, 31, 33, 100, 257, 1000, 4096, 6144, 28672, 128256]
 COLS = [256, 1024, 2048, 3072, 3328, 4096, 14336]
 
 
-@pytest.mark.parametrize("fmt", [8, 4, 1])
+@pytest.mark.parametrize("fmt", [8, 4, 75, 1])
 def test_plan_invariants(hq, fmt):
     chunk = 128 if fmt == 1 else 256
     for rows, cols, n_vec in itertools.product(ROWS, COLS, range(1, 9)):
@@ -90,13 +96,13 @@ def test_plan_invariants(hq, fmt):
         p = plan(hq, fmt, n_vec, rows, cols, regs)
         what = f"fmt {fmt} {rows}x{cols} n_vec={n_vec}: {p}"
         n_chunks = cols // chunk
-        assert p["policy"] == expected_policy(fmt, n_vec, cols), what
-        rpl = 2 if (fmt == 4 and n_vec <= 2) else 1
+        assert p["policy"] == expected_policy(fmt, n_vec, rows, cols), what
+        rpl = 2 if (fmt in (4, 75) and n_vec <= 2) else 1
         assert p["tile_rows"] == 32 * rpl * (p["cons_warps"] if p["policy"] == 3 else 1), what
         assert p["tiles"] == math.ceil(rows / p["tile_rows"]), what
         # the ring: one owner per stage (a multiple of the consumer warps), or at
         # least a double buffer when every warp consumes every stage
-        if p["policy"] == 3:
+        if p["policy"] in (3, 4):
             assert p["stages"] >= 2, what
         else:
             assert p["stages"] >= p["cons_warps"] and p["stages"] % p["cons_warps"] == 0, what
