@@ -457,16 +457,15 @@ class Step:
             elif op.kind == "dense":
                 fn = {"q8_0": hq.hq_matvec_q8_0, "q4_0": hq.hq_matvec_q4_0, "q4_k": hq.hq_matvec_q4_k}[op.fmt]
                 fn(self.W[i], self.x[i], self.y[i], op.rows, op.cols, n_vec, stream=stream)
-            elif op.kind == "moe" and op.epi == "swiglu":
-                hq.hq_moe_matvec_q8_0_swiglu(self.W[i], self.ids[i], self.x[i], op.x_per_slot, self.y[i],
-                                             op.n_experts, op.n_active, op.rows, op.cols, n_vec, stream=stream)
-            elif op.kind == "moe" and op.epi == "combine":
-                hq.hq_moe_matvec_q8_0_combine(self.W[i], self.ids[i], self.x[i], op.x_per_slot, self.comb[i],
-                                              self.y[i], op.n_experts, op.n_active, op.rows, op.cols, n_vec,
-                                              stream=stream)
             elif op.kind == "moe":
-                hq.hq_moe_matvec_q8_0(self.W[i], self.ids[i], self.x[i], op.x_per_slot, self.y[i],
-                                      op.n_experts, op.n_active, op.rows, op.cols, n_vec, stream=stream)
+                # a layer's down launch uses the ids its gate|up launch used: they were written
+                # before the launch that precedes it, so its weight copies may start early
+                epi = {None: hq.HQ_MOE_EPI_NONE, "swiglu": hq.HQ_MOE_EPI_SWIGLU,
+                       "combine": hq.HQ_MOE_EPI_COMBINE}[op.epi]
+                flags = hq.HQ_MOE_IDS_READY if op.label == "down" else 0
+                hq.hq_moe_matvec_q8_0_ex(self.W[i], self.ids[i], self.x[i], op.x_per_slot, self.comb[i],
+                                         self.y[i], op.n_experts, op.n_active, op.rows, op.cols, n_vec, epi,
+                                         flags, stream=stream)
             else:
                 hq.hq_matvec_i8_requant(self.W[i], self.x[i], self.mult[i], self.shift[i], self.y[i],
                                         op.rows, op.cols, n_vec, stream=stream)

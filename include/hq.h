@@ -274,6 +274,35 @@ hq_status hq_moe_matvec_q8_0_combine(const void *W_bank, const int32_t *expert_i
                                      int n_active, int64_t rows, int64_t cols, int n_vec, hq_stream_t stream);
 
 /*
+ * hq_moe_matvec_q8_0_ex -- the three MoE calls above in one entry point, with
+ * flags.
+ *   epilogue : HQ_MOE_EPI_NONE (as hq_moe_matvec_q8_0; router_w unused),
+ *              HQ_MOE_EPI_SWIGLU (as hq_moe_matvec_q8_0_swiglu) or
+ *              HQ_MOE_EPI_COMBINE (as hq_moe_matvec_q8_0_combine).
+ *   flags    : 0, or HQ_MOE_IDS_READY: the caller guarantees that expert_ids
+ *              were written by work that completed before the kernel that
+ *              precedes this call in the stream -- e.g. the down projection of
+ *              an MoE feed-forward, whose ids the router wrote before the
+ *              gate|up launch.  The kernel then reads the ids and starts its
+ *              weight copies while that kernel is still running, waiting for
+ *              it only before it reads x or writes y.  Ids written by the
+ *              immediately preceding kernel break the guarantee (the kernel
+ *              may read stale ids).
+ * All other arguments, results and errors as for the calls above; unknown
+ * epilogues or flags give HQ_ERR_UNSUPPORTED.
+ * Source: as hq_moe_matvec_q8_0 ("One Native Stack ...", section "The
+ * Unified Quant Core": every routed expert through the same core; "Economical
+ * Serving ...", subsection "The Roofline that Sets the Price").
+ */
+#define HQ_MOE_EPI_NONE 0
+#define HQ_MOE_EPI_SWIGLU 1
+#define HQ_MOE_EPI_COMBINE 2
+#define HQ_MOE_IDS_READY 1
+hq_status hq_moe_matvec_q8_0_ex(const void *W_bank, const int32_t *expert_ids, const float *x, int x_per_slot,
+                                const float *router_w, float *y, int64_t n_experts, int n_active, int64_t rows,
+                                int64_t cols, int n_vec, int epilogue, int flags, hq_stream_t stream);
+
+/*
  * Quantizers (the one-off data-preparation step, on the GPU).
  * hq_quantize_q8_0: W fp32 [rows][cols] (device) -> out Q8_0 blocks (device):
  *   d = max|w|/127 in fp32, stored fp16 (round to nearest even);

@@ -18,7 +18,8 @@ from ._binding import (  # noqa: F401
     lib, lib_path, hq_version, hq_last_error,
     hq_matvec_q8_0, hq_matvec_q4_0, hq_matvec_i8_requant, hq_moe_matvec_q8_0,
     hq_matvec_q4_k, hq_quantize_q4_k, FMT_CODES, QK_K, Q4_K_BLOCK_BYTES,
-    hq_moe_matvec_q8_0_swiglu, hq_moe_matvec_q8_0_combine,
+    hq_moe_matvec_q8_0_swiglu, hq_moe_matvec_q8_0_combine, hq_moe_matvec_q8_0_ex,
+    HQ_MOE_EPI_NONE, HQ_MOE_EPI_SWIGLU, HQ_MOE_EPI_COMBINE, HQ_MOE_IDS_READY,
     hq_matvec_q8_0_lora, hq_matvec_q4_0_lora, hq_matvec_q8_0_lora_noalloc,
     hq_quantize_q8_0, hq_quantize_q4_0, hq_quantize_i8_rows, hq_requant_params,
     hq_requant_i32_debug, hq_device_fault, hq_selftest_wait_timeout, hq_launch_count, hq_debug_plan,

@@ -59,6 +59,7 @@ _SIGS = {
     "hq_moe_matvec_q8_0": ([_vp, _vp, _vp, _int, _vp, _i64, _int, _i64, _i64, _int, _vp], _int),
     "hq_moe_matvec_q8_0_swiglu": ([_vp, _vp, _vp, _int, _vp, _i64, _int, _i64, _i64, _int, _vp], _int),
     "hq_moe_matvec_q8_0_combine": ([_vp, _vp, _vp, _int, _vp, _vp, _i64, _int, _i64, _i64, _int, _vp], _int),
+    "hq_moe_matvec_q8_0_ex": ([_vp, _vp, _vp, _int, _vp, _vp, _i64, _int, _i64, _i64, _int, _int, _int, _vp], _int),
     "hq_quantize_q8_0": ([_vp, _vp, _i64, _i64, _vp], _int),
     "hq_quantize_q4_0": ([_vp, _vp, _i64, _i64, _vp], _int),
     "hq_quantize_i8_rows": ([_vp, _vp, _vp, _i64, _i64, _vp], _int),
@@ -197,6 +198,17 @@ def hq_moe_matvec_q8_0_combine(W_bank, expert_ids, x, x_per_slot: int, router_w,
     return _check(lib().hq_moe_matvec_q8_0_combine(_addr(W_bank), _addr(expert_ids), _addr(x), int(x_per_slot),
                                                    _addr(router_w), _addr(y), n_experts, n_active, rows, cols,
                                                    n_vec, _stream(stream)))
+
+
+HQ_MOE_EPI_NONE, HQ_MOE_EPI_SWIGLU, HQ_MOE_EPI_COMBINE = 0, 1, 2
+HQ_MOE_IDS_READY = 1
+
+
+def hq_moe_matvec_q8_0_ex(W_bank, expert_ids, x, x_per_slot: int, router_w, y, n_experts: int, n_active: int,
+                          rows: int, cols: int, n_vec: int, epilogue: int, flags: int, stream=None) -> int:
+    return _check(lib().hq_moe_matvec_q8_0_ex(_addr(W_bank), _addr(expert_ids), _addr(x), int(x_per_slot),
+                                              _addr(router_w), _addr(y), n_experts, n_active, rows, cols, n_vec,
+                                              int(epilogue), int(flags), _stream(stream)))
 
 
 def hq_quantize_q8_0(W, out, rows: int, cols: int, stream=None) -> int:

@@ -294,6 +294,28 @@ hq_status hq_moe_matvec_q8_0_combine(const void *W_bank, const int32_t *expert_i
                                   n_vec, &e, (cudaStream_t)stream));
 }
 
+hq_status hq_moe_matvec_q8_0_ex(const void *W_bank, const int32_t *expert_ids, const float *x, int x_per_slot,
+                                const float *router_w, float *y, int64_t n_experts, int n_active, int64_t rows,
+                                int64_t cols, int n_vec, int epilogue, int flags, hq_stream_t stream) {
+    hq_status st = check_moe(W_bank, expert_ids, x, x_per_slot, y, n_experts, n_active, rows, cols, n_vec);
+    if (st != HQ_OK) return st;
+    if (epilogue < HQ_MOE_EPI_NONE || epilogue > HQ_MOE_EPI_COMBINE)
+        return set_error(HQ_ERR_UNSUPPORTED, "epilogue %d is not HQ_MOE_EPI_NONE, _SWIGLU or _COMBINE", epilogue);
+    if (flags & ~HQ_MOE_IDS_READY) return set_error(HQ_ERR_UNSUPPORTED, "unknown flags %#x", flags);
+    if (epilogue == HQ_MOE_EPI_SWIGLU && rows % 2 != 0)
+        return set_error(HQ_ERR_SHAPE, "SwiGLU needs interleaved gate/up rows: rows = %lld is odd", (long long)rows);
+    if (epilogue == HQ_MOE_EPI_COMBINE) {
+        if (!router_w) return set_error(HQ_ERR_NULL, "router_w must be non-null");
+        if (!aligned(router_w, 4)) return set_error(HQ_ERR_ALIGN, "router_w must be 4-byte aligned");
+    }
+    MoeEpi e;
+    e.kind = epilogue;
+    e.router_w = epilogue == HQ_MOE_EPI_COMBINE ? router_w : nullptr;
+    e.ids_ready = (flags & HQ_MOE_IDS_READY) ? 1 : 0;
+    return finish(launch_moe_q8_0(W_bank, expert_ids, x, x_per_slot, y, n_experts, n_active, rows, cols,
+                                  n_vec, &e, (cudaStream_t)stream));
+}
+
 hq_status hq_quantize_q8_0(const float *W, void *out, int64_t rows, int64_t cols, hq_stream_t stream) {
     if (!W || !out) return set_error(HQ_ERR_NULL, "W and out must be non-null");
     if (rows < 1 || cols < 32 || cols % 32 != 0) return set_error(HQ_ERR_SHAPE, "need rows>=1, cols%%32==0");

@@ -48,6 +48,7 @@ hq_status launch_lora_down(const uint16_t *A, const float *x, float *u, int rank
 struct MoeEpi {
     int kind = 0;
     const float *router_w = nullptr;    // [n_vec][n_active]
+    int ids_ready = 0;                  // the ids do not come from the previous kernel in the stream
 };
 hq_status launch_moe_q8_0(const void *W_bank, const int32_t *ids, const float *x, int x_per_slot,
                           float *y, int64_t n_experts, int n_active, int64_t rows, int64_t cols,

@@ -543,6 +543,7 @@ struct KArgs {
     const float *router_w;    //   combine: router weights [n_vec][n_active]
     int gsplit;               // combine: CTAs per row tile (a cluster when > 1), over the tile's expert groups
     int lay_ks;               // gather-buffer slots in the shared-memory layout
+    int ids_ready;            // MoE: the expert ids were written before the previous kernel in the stream
 };
 
 // MoE epilogues.  SwiGLU: an expert's gate and up rows are interleaved (row 2i
@@ -741,8 +742,9 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
     }
     griddep_launch_dependents();
     if constexpr (MOE) {
-        // ids may come from the previous kernel (a router): wait for it first
-        griddep_wait();
+        // ids may come from the previous kernel (a router): wait for it first,
+        // unless the caller vouches that they were written before it
+        if (!a.ids_ready) griddep_wait();
         // Group the (token, slot) pairs by expert; every CTA derives the same
         // table.  The ids are read from global memory once, in parallel, and
         // every later look-up is a shared-memory read.
@@ -772,10 +774,12 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 i = j;
             }
             *mt.n_groups = ng;
+            misc[2] = bad;
             if (bad && blockIdx.x == 0) atomicOr(a.fault, kFaultExpertId);
         }
         __syncthreads();
-        if (blockIdx.x == 0) {                     // outputs of invalid ids become NaN
+        if (blockIdx.x == 0 && misc[2]) {          // outputs of invalid ids become NaN
+            if (a.ids_ready) griddep_wait();       // y may still be in use by the previous kernel
             const long long out_rows = a.moe_epi == kEpiSwiglu ? a.rows / 2 : a.rows;
             for (int p = 0; p < P_ && a.moe_epi != kEpiCombine; ++p) {   // combine: the leader writes NaN sums
                 const int e = mt.ids[p];
@@ -812,14 +816,22 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
             // weight tiles are requested at once, and only then does the producer
             // wait for the previous kernel (x and the expert ids may come from it).
             uint32_t n_pre = 0;
-            if (!MOE) {
-                for (int work = work0; work < n_work && n_pre < (uint32_t)S; work += wstep)
+            if (!MOE || a.ids_ready) {
+                for (int work = work0; work < n_work && n_pre < (uint32_t)S; work += wstep) {
+                    long long row0 = (long long)(work % a.num_tiles) * TR;
+                    int m = NV;
+                    if (MOE) {
+                        const int g = work / a.num_tiles;
+                        m = mt.gsize[g];
+                        row0 += (long long)mt.gexpert[g] * a.rows;
+                    }
                     for (int j = 0; j < nloc && n_pre < (uint32_t)S; ++j, ++n_pre) {
                         const uint32_t fb = smem_u32(&full[n_pre]);
-                        mbar_arrive_expect_tx(fb, WT + NV * XV);
+                        mbar_arrive_expect_tx(fb, WT + m * XV);
                         tma_load_2d(smem_u32(smem + (size_t)n_pre * ST), &a.tmW, (k0 + j) * P::kBoxInner,
-                                    (int)((long long)(work % a.num_tiles) * TR), fb, polW);
+                                    (int)row0, fb, polW);
                     }
+                }
                 griddep_wait();
             }
             uint32_t n = 0;
@@ -1602,6 +1614,7 @@ hq_status moe_nv(const DeviceInfo &dev, const void *W_bank, const int32_t *ids, 
     a.x_per_slot = x_per_slot;
     a.moe_epi = epi.kind;
     a.router_w = epi.router_w;
+    a.ids_ready = epi.ids_ready;
     if (epi.kind == kEpiCombine) {
         // G CTAs per row tile over the tile's expert groups: the largest G
         // (at most kCombineCluster) whose clusters all fit in one wave, as the

@@ -73,6 +73,13 @@ def test_host_validation_before_any_launch(hq):
     assert L.hq_moe_matvec_q8_0_combine(fake, fake, fake, 1, 0, fake, 4, 2, 8, 256, 1, 0) == hq.HQ_ERR_NULL
     assert L.hq_moe_matvec_q8_0_combine(fake, fake, fake, 1, fake + 2, fake, 4, 2, 8, 256, 1, 0) == hq.HQ_ERR_ALIGN
     assert L.hq_moe_matvec_q8_0_combine(fake, fake, fake, 1, fake, fake, 4, 5, 8, 256, 1, 0) == hq.HQ_ERR_SHAPE
+    # MoE with flags: unknown epilogues and flags are refused, the combine needs its weights
+    Le = L.hq_moe_matvec_q8_0_ex
+    assert Le(fake, fake, fake, 0, 0, fake, 4, 2, 8, 256, 1, 3, 0, 0) == hq.HQ_ERR_UNSUPPORTED
+    assert Le(fake, fake, fake, 0, 0, fake, 4, 2, 8, 256, 1, 0, 2, 0) == hq.HQ_ERR_UNSUPPORTED
+    assert Le(fake, fake, fake, 1, 0, fake, 4, 2, 8, 256, 1, 2, 1, 0) == hq.HQ_ERR_NULL
+    assert Le(fake, fake, fake, 0, 0, fake, 4, 2, 9, 256, 1, 1, 1, 0) == hq.HQ_ERR_SHAPE
+    assert Le(fake, fake, fake, 0, 0, fake, 4, 5, 8, 256, 1, 0, 1, 0) == hq.HQ_ERR_SHAPE
     # Q4_K: super-blocks of 256 columns, W and x 16-byte aligned
     assert L.hq_matvec_q4_k(fake, fake, fake, 4, 288, 1, 0) == hq.HQ_ERR_SHAPE
     assert L.hq_matvec_q4_k(fake, fake, fake, 4, 224, 1, 0) == hq.HQ_ERR_SHAPE

@@ -76,10 +76,14 @@ def test_dense_chain_in_graph(hq):
             x_in = y_np
 
 
-def test_moe_chain_with_device_ids_in_graph(hq):
+@pytest.mark.parametrize("down_flags", [0, 1])
+def test_moe_chain_with_device_ids_in_graph(hq, down_flags):
     """A small kernel writes the expert ids right before the MoE gate launch,
     and the down launch reads the gate launch's output as its per-slot x; the
-    whole chain is captured and replayed with two different routings."""
+    whole chain is captured and replayed with two different routings.  With
+    HQ_MOE_IDS_READY on the down launch (its ids were written before the gate
+    launch), the down kernel reads the ids and starts its weight copies while
+    the gate launch still runs, and must still take x only after it ends."""
     E, A, H, F = 128, 8, 2048, 768
     g = synthetic.rng(4343)
     gate = np.empty((E * F, H // 32 * 34), np.uint8)
@@ -98,7 +102,8 @@ def test_moe_chain_with_device_ids_in_graph(hq):
     def launch(stream):
         torch.remainder(seed + step, E, out=ids.view(-1))          # ids written on the device
         hq.hq_moe_matvec_q8_0(gate_d, ids, x, 0, y_gate, E, A, F, H, 1, stream=stream)
-        hq.hq_moe_matvec_q8_0(down_d, ids, y_gate, 1, y_down, E, A, H, F, 1, stream=stream)
+        hq.hq_moe_matvec_q8_0_ex(down_d, ids, y_gate, 1, None, y_down, E, A, H, F, 1, hq.HQ_MOE_EPI_NONE,
+                                 down_flags, stream=stream)
 
     s = torch.cuda.Stream()
     with torch.cuda.stream(s):
@@ -119,7 +124,7 @@ def test_moe_chain_with_device_ids_in_graph(hq):
         yg_ref, Tg = oracle.moe_matvec_q8_0(gate, ids_np, x.cpu().numpy(), False, E, A, F, H, 1)
         assert_within(yg, yg_ref, Tg, f"moe gate, routing {base}")
         yd_ref, Td = oracle.moe_matvec_q8_0(down, ids_np, yg.reshape(A, F), True, E, A, H, F, 1)
-        assert_within(y_down.cpu().numpy(), yd_ref, Td, f"moe down, routing {base}")
+        assert_within(y_down.cpu().numpy(), yd_ref, Td, f"moe down (flags {down_flags}), routing {base}")
     assert hq.hq_device_fault() == 0
 
 
