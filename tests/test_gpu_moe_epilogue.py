@@ -189,11 +189,14 @@ def test_invalid_ids_in_epilogues(hq):
     assert np.all(np.isnan(y))
 
 
-def test_moe_ffn_chain_in_graph(hq):
+@pytest.mark.parametrize("down_flags", [0, 1])
+def test_moe_ffn_chain_in_graph(hq, down_flags):
     """Two MoE feed-forward layers, each gate|up + SwiGLU then down + combine,
     the next layer reading the previous layer's combined output, captured in a
     CUDA graph and replayed with two different inputs and routings.  Each stage
-    is checked against the oracle on the GPU's own input to that stage."""
+    is checked against the oracle on the GPU's own input to that stage.  With
+    HQ_MOE_IDS_READY the down launches (their ids were written before the
+    gate|up launch) start their weight copies before gate|up ends."""
     n_experts, n_active, hidden, inter, n_vec = 16, 4, 512, 256, 2
     g = synthetic.rng(6300)
     layers = []
@@ -214,8 +217,8 @@ def test_moe_ffn_chain_in_graph(hq):
         for li, (_, _, gud, downd) in enumerate(layers):
             hq.hq_moe_matvec_q8_0_swiglu(gud, ids_d[li], xin, 0, h_d[li], n_experts, n_active, 2 * inter, hidden,
                                          n_vec, stream=s.cuda_stream)
-            hq.hq_moe_matvec_q8_0_combine(downd, ids_d[li], h_d[li], 1, w_d[li], out_d[li],
-                                          n_experts, n_active, hidden, inter, n_vec, stream=s.cuda_stream)
+            hq.hq_moe_matvec_q8_0_ex(downd, ids_d[li], h_d[li], 1, w_d[li], out_d[li], n_experts, n_active,
+                                     hidden, inter, n_vec, hq.HQ_MOE_EPI_COMBINE, down_flags, stream=s.cuda_stream)
             xin = out_d[li]
 
     with torch.cuda.stream(s):
