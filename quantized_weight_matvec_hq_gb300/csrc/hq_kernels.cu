@@ -1132,45 +1132,37 @@ __global__ void requant_debug_kernel(const int32_t *__restrict__ acc, const int3
 }
 
 // QLoRA down projection u[v][k] = sum_j A[k][j] * x[v][j] (A bf16 [rank][cols],
-// cols % 8 == 0): one CTA per adapter row k, eight columns per thread and
-// step, then a fixed-order reduction (warp shuffles, then the warps in order),
-// so u is the same bit for bit on every run.  Launched as a programmatic
-// dependent: it becomes resident while the previous kernel drains, loads its
-// row of A, and reads x (which that kernel may write) only after waiting for
-// it; it lets the matvec that follows start at once (that kernel reads u only
-// after waiting for this one).
-__global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t *__restrict__ A,
-                                                        const float *__restrict__ x, float *__restrict__ u,
-                                                        int rank, long long cols, int n_vec) {
+// cols % 8 == 0): one CTA of 512 threads per adapter row k, eight columns per
+// thread and step, so a row of up to 4096 columns is one step and of up to
+// 8192 two; then a fixed-order reduction (warp shuffles, then the 16 warps in
+// order), so u is the same bit for bit on every run.  Launched as a
+// programmatic dependent: it becomes resident while the previous kernel
+// drains, loads its first two steps of A, and reads x (which that kernel may
+// write) only after waiting for it; both steps' x loads are then in flight at
+// once.  It lets the matvec that follows start at once (that kernel reads u
+// only after waiting for this one).  Against one CTA of 256 threads with a
+// step at a time: 8B token with rank-16 adapters 3821 -> 3937 GB/s (Q8_0),
+// 2294 -> 2330 (Q4_0); 1024 threads gained more on Q4_0 (2381) but lost on
+// Q8_0 (3789): a larger CTA holds more of the SM the overlapping matvec needs.
+constexpr int kLoraThreads = 512;
+__global__ void __launch_bounds__(kLoraThreads) lora_down_kernel(const uint16_t *__restrict__ A,
+                                                                 const float *__restrict__ x,
+                                                                 float *__restrict__ u, int rank, long long cols,
+                                                                 int n_vec) {
     griddep_launch_dependents();
     const int k = blockIdx.x;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint4 *a8 = reinterpret_cast<const uint4 *>(A + (long long)k * cols);
     const long long n8 = cols / 8;
-    // A is a weight: its row is read before waiting for the previous kernel
-    // (up to 8 x 8 columns per thread, i.e. cols <= 16384, held in registers)
-    constexpr int kPre = 8;
-    uint4 pre[kPre];
-#pragma unroll
-    for (int i = 0; i < kPre; ++i) {
-        const long long c = threadIdx.x + (long long)i * blockDim.x;
-        pre[i] = c < n8 ? a8[c] : make_uint4(0u, 0u, 0u, 0u);
-    }
+    // A is a weight: its first two steps are read before waiting for the previous kernel
+    const long long c0 = threadIdx.x, c1 = threadIdx.x + kLoraThreads;
+    const uint4 w0 = c0 < n8 ? a8[c0] : make_uint4(0u, 0u, 0u, 0u);
+    const uint4 w1 = c1 < n8 ? a8[c1] : make_uint4(0u, 0u, 0u, 0u);
     griddep_wait();
     float acc[8];
 #pragma unroll
     for (int v = 0; v < 8; ++v) acc[v] = 0.f;
-    int i = 0;
-    for (long long c = threadIdx.x; c < n8; c += blockDim.x, ++i) {
-        uint4 w;
-        if (i < kPre) {
-            // select the prefetched word without a dynamic register index
-            w = pre[0];
-#pragma unroll
-            for (int t = 1; t < kPre; ++t) if (t == i) w = pre[t];
-        } else {
-            w = a8[c];
-        }
+    auto step = [&](const uint4 &w, long long c) {
         const float wf[8] = {__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
                              __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u),
                              __uint_as_float(w.z << 16), __uint_as_float(w.z & 0xffff0000u),
@@ -1185,8 +1177,11 @@ __global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t *__restri
             t = fmaf(wf[4], q.x, t); t = fmaf(wf[5], q.y, t); t = fmaf(wf[6], q.z, t); t = fmaf(wf[7], q.w, t);
             acc[v] = t;
         }
-    }
-    __shared__ float red[8][8];
+    };
+    if (c0 < n8) step(w0, c0);
+    if (c1 < n8) step(w1, c1);
+    for (long long c = c1 + kLoraThreads; c < n8; c += kLoraThreads) step(a8[c], c);
+    __shared__ float red[kLoraThreads / 32][8];
 #pragma unroll
     for (int v = 0; v < 8; ++v) {
         float t = acc[v];
@@ -1196,7 +1191,7 @@ __global__ void __launch_bounds__(256) lora_down_kernel(const uint16_t *__restri
     __syncthreads();
     if (threadIdx.x < n_vec) {
         float t = 0.f;
-        for (int w2 = 0; w2 < (int)(blockDim.x >> 5); ++w2) t += red[w2][threadIdx.x];
+        for (int w2 = 0; w2 < kLoraThreads / 32; ++w2) t += red[w2][threadIdx.x];
         u[(long long)threadIdx.x * rank + k] = t;
     }
 }
@@ -1285,6 +1280,16 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     int ks = 1;
     p.slots = slots;
     while (gsplit == 0 && ks < kMaxSplit && n_work * ks * 2 <= slots && n_chunks >= 2 * ks) ks *= 2;
+    // Q4_0 (decode-bound) on launches short enough that the largest K split
+    // that still fits one wave leaves each CTA at most three chunks: that split
+    // fills every CTA slot (o 4096x4096: clusters of 7, 1626 -> 1880 GB/s; the
+    // 8B token 2990 -> 3056).  Longer rows lost with it (down 4096x14336, 8
+    // chunks per CTA: 2872 -> 2529), and so did Q4_K (token 2553 -> 2171).
+    if (std::is_same<P, PolQ4_0>::value && gsplit == 0 && ks > 1 && !MOE) {
+        int kf = ks;
+        while (kf < kMaxSplit && n_work * (kf + 1) <= slots && n_chunks >= kf + 1) ++kf;
+        if ((n_chunks + kf - 1) / kf <= 3) ks = kf;
+    }
     p.ksplit = ks;
     p.gsplit = std::max(gsplit, 1);
     // gather-buffer slots: the K split's partials, or a combine's own partial sums
@@ -1500,11 +1505,13 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
         // owner per stage: with its 128-row split stages it measured 1866 / 1605 /
         // 1007 -> 1794 / 1586 / 926 GB/s at n_vec 3 / 4 / 8.
         return f(PolRowSplit<P>{}, RT{});
-    } else if constexpr (P::kNibbles && NV == 1) {
+    } else if constexpr (P::kNibbles && (NV == 1 || (NV == 2 && std::is_same<P, PolQ4_0>::value))) {
         // column-split stages where the launch does not split K over clusters
         // (enough 64-row tiles to give every CTA slot two): Q4_0 gate|up
         // 28672x4096 3386 -> 3635 GB/s; with a K split they lost (o 4096x4096
-        // 1622 -> 1482, down 4096x14336 2877 -> 2413 GB/s)
+        // 1622 -> 1482, down 4096x14336 2877 -> 2413 GB/s).  At two vectors
+        // the Q4_0 token gained (2137 -> 2277 GB/s) and the Q4_K token lost
+        // (1995 -> 1885), whose decode holds more registers per row.
         constexpr int TR = 32 * R;
         const bool k_split = (rows + TR - 1) / TR * 2 <= (long long)dev.num_sms * ctas_per_sm<P, NV, R>();
         if (!k_split) return f(PolColSplit<P>{}, RT{});
@@ -1709,7 +1716,7 @@ hq_status launch_lora_down(const uint16_t *A, const float *x, float *u, int rank
                            int n_vec, cudaStream_t stream) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)rank, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
+    cfg.blockDim = dim3(kLoraThreads, 1, 1);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

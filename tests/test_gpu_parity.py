@@ -421,11 +421,23 @@ def test_moe_all_same_expert_equals_dense(hq):
         assert_within(y[:, k], y_ref, T, f"moe slot {k}")
 
 
-def test_moe_invalid_id_sets_fault_and_nan(hq):
+@pytest.mark.parametrize("flags", [0, 1])
+def test_moe_invalid_id_sets_fault_and_nan(hq, flags):
+    """An out-of-range expert id: NaN rows for its slots, the fault bit, exact
+    neighbours -- also when the launch reads its ids before waiting for the
+    previous kernel (HQ_MOE_IDS_READY), where the NaN rows must still be
+    written only after that wait."""
     n_experts, n_active, rows, cols, n_vec = 4, 2, 64, 256, 2
     bank, _, x = _moe_case(n_experts, n_active, rows, cols, n_vec, 4002, False)
     ids = np.array([[1, 9], [3, -1]], dtype=np.int32)
-    y = gpu_moe(hq, bank, ids, x, False, n_experts, n_active, rows, cols, n_vec)
+    if flags:
+        yd = torch.full((n_vec, n_active, rows), 7.0, dtype=torch.float32, device="cuda")
+        hq.hq_moe_matvec_q8_0_ex(dev(bank), dev(ids), dev(x), 0, None, yd, n_experts, n_active, rows, cols,
+                                 n_vec, hq.HQ_MOE_EPI_NONE, hq.HQ_MOE_IDS_READY)
+        torch.cuda.synchronize()
+        y = yd.cpu().numpy()
+    else:
+        y = gpu_moe(hq, bank, ids, x, False, n_experts, n_active, rows, cols, n_vec)
     assert hq.hq_device_fault() == hq.HQ_FAULT_EXPERT_ID
     assert np.all(np.isnan(y[0, 1])) and np.all(np.isnan(y[1, 1]))
     ok = np.array([[1, 0], [3, 0]], dtype=np.int32)
@@ -461,7 +473,9 @@ def test_q8_0_launch_policy_boundaries(hq, rows, cols, n_vec):
     # one vector: K split over clusters up to 228 tiles of 64 rows on 152 SMs,
     # column-split stages from 229 tiles on (ragged last tiles both sides)
     ("q4_0", 14592, 512, 1), ("q4_0", 14593, 512, 1), ("q4_0", 20000, 768, 1),
-    ("q4_k", 14592, 512, 1), ("q4_k", 14593, 512, 1)])
+    ("q4_k", 14592, 512, 1), ("q4_k", 14593, 512, 1),
+    # Q4_0 at two vectors: column-split stages too (Q4_K keeps one stage per warp there)
+    ("q4_0", 14592, 512, 2), ("q4_0", 14593, 512, 2), ("q4_k", 14593, 512, 2)])
 def test_nibble_launch_policy_boundaries(hq, fmt, rows, cols, n_vec):
     """Q4_0 / Q4_K at one vector (four consumer warps: one stage per warp with a
     K split, column-split stages without) and at five vectors (three CTAs per

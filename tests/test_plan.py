@@ -54,7 +54,7 @@ PINS = [
     ((8, 1, 4096, 4096, 80), (512, 96, 4, 39904)),       # Q8_0 o (full capture)
     ((4, 1, 4096, 14336, 97), (256, 160, 4, None)),
     ((4, 1, 6144, 4096, 97), (384, 160, 4, None)),
-    ((4, 1, 4096, 4096, 97), (256, 160, 4, None)),
+    ((4, 1, 4096, 4096, 97), (448, 160, 7, None)),      # Q4_0 o: the K split that fills one wave
     ((4, 1, 128256, 4096, 97), (456, 160, 1, None)),
 ]
 
@@ -77,7 +77,7 @@ def expected_policy(fmt, n_vec, rows, cols):
         return 2
     if fmt == 8:
         return 3
-    if fmt in (4, 75) and n_vec == 1:
+    if (fmt in (4, 75) and n_vec == 1) or (fmt == 4 and n_vec == 2):
         # column-split stages unless K is split over clusters (64-row tiles too
         # few to give each of the 152 x 3 CTA slots two)
         return 4 if math.ceil(rows / 64) * 2 > GB300["num_sms"] * 3 else 0
