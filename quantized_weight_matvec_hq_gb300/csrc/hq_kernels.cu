@@ -85,8 +85,8 @@ struct PolQ8_0 {
     static constexpr int kConsWarps = 2;            // memory-bound: few warps per CTA, more CTAs
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
-    static constexpr bool kRowSplit = false;        // see PolRowSplit
     static constexpr bool kColSplit = false;        // see PolColSplit
+    static constexpr bool kRuntimeCols = false;     // consume_pair, see PolQ8_0Wide
     static constexpr bool kNibbles = false;         // 4-bit quants (decode-bound launch policies)
     using Acc = float2;
     using Red = float;
@@ -194,6 +194,82 @@ struct PolQ8_0Two : PolQ8_0 {
     static constexpr int kConsWarpsFewAcc = 3;
 };
 
+// Q8_0 at three or more vectors: the block scale is folded into each weight,
+// so a lane carries several rows without per-block partial sums (their
+// registers would go to the rows instead), and x, loaded once per column
+// group, serves every row of the lane.  The quant byte u = q + 128 is placed
+// by one prmt at bits 8..15 of 2^23: the fp32 value f = 2^23 + 256 u.  With
+// d' = d / 256 one packed fma gives f d' - (2^23 + 2^15) d' = q d exactly:
+// (2^23 + 2^15) d' = 257 * 2^7 * d has 9 + 11 significant bits and q d has
+// 8 + 11, so both are representable and the fma's one rounding of its exact
+// result is none.  The running sums then hold partial sums of w x only.
+__device__ __forceinline__ float byte_mid_as_float(uint32_t word, int byte) {
+    // 2^23 + 256 * (byte `byte` of `word`)
+    return __uint_as_float(prmt(word, kMagic, 0x7604u | ((uint32_t)byte << 4)));
+}
+
+struct PolQ8_0Wide : PolQ8_0 {
+    static constexpr int kConsWarps = 4;            // column split: each warp two blocks of every stage
+    static constexpr int kConsWarpsFewAcc = 4;
+    static constexpr bool kComputeBound = true;     // the FP32 pipe, not HBM, sets the pace at eight vectors
+    static constexpr bool kRuntimeCols = true;      // see consume_pair
+
+    // Blocks 2p and 2p + 1 of the stage's chunk for R rows per lane.  The pair
+    // is 68 bytes from byte 68p of each row chunk: 17 words from a 4-byte
+    // aligned start, the same word and byte positions for every p.  So p is a
+    // run-time value and one copy of this code serves all four warps of a
+    // column split (four copies with constant offsets overflow the SM's
+    // instruction cache at these unroll depths).
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume_pair(const uint8_t *__restrict__ wt,
+                                                        const uint8_t *__restrict__ xt8, int lane, int p,
+                                                        Acc (&acc)[R][NV]) {
+        const float *xt = reinterpret_cast<const float *>(xt8) + 64 * p;
+        uint32_t w[R][17];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t *rp = reinterpret_cast<const uint32_t *>(wt + (lane + 32 * r) * kChunkBytes + 68 * p);
+#pragma unroll
+            for (int k = 0; k < 17; ++k) w[r][k] = rp[k] ^ 0x80808080u;   // quant bytes q + 128 (and d's bytes flipped)
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float2 dd[R], cc[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const unsigned short hb = (unsigned short)((h ? (w[r][8] >> 16) : (w[r][0] & 0xffffu)) ^ 0x8080u);
+                const float dq = __half2float(__ushort_as_half(hb)) * 0.00390625f;   // d / 256, exact
+                const float c = -8421376.0f * dq;                                   // -(2^23 + 2^15) d / 256, exact
+                dd[r] = make_float2(dq, dq);
+                cc[r] = make_float2(c, c);
+            }
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                float4 xv[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * h + 4 * g);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    float f[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int o = 34 * h + 2 + 4 * g + i;     // byte of quant 4g+i in the pair
+                        f[i] = byte_mid_as_float(w[r][o >> 2], o & 3);
+                    }
+                    const float2 w01 = ffma2(make_float2(f[0], f[1]), dd[r], cc[r]);
+                    const float2 w23 = ffma2(make_float2(f[2], f[3]), dd[r], cc[r]);
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        acc[r][v] = ffma2(w01, make_float2(xv[v].x, xv[v].y), acc[r][v]);
+                        acc[r][v] = ffma2(w23, make_float2(xv[v].z, xv[v].w), acc[r][v]);
+                    }
+                }
+            }
+        }
+    }
+};
+
 // Q4_0 nibble decode, one and-or per element: a nibble at bit p in {0, 4, 8,
 // 12}, masked in place and ORed into the exponent of 2^23, is the fp32 value
 // 2^23 + n * 2^p (exact: the mantissa has 23 bits); adding -(2^23 + 8 * 2^p)
@@ -229,8 +305,8 @@ struct PolQ4_0 {
     static constexpr int kConsWarps = 4;            // nibble decode is ALU-heavy: more warps hide its latency
     static constexpr int kConsWarpsFewAcc = 4;      // n_vec 1 (two rows per lane; see make_plan's ring)
     static constexpr bool kComputeBound = true;     // decode, not HBM, sets the pace
-    static constexpr bool kRowSplit = false;
     static constexpr bool kColSplit = false;
+    static constexpr bool kRuntimeCols = false;     // consume_pair, see PolQ8_0Wide
     static constexpr bool kNibbles = true;
     using Acc = float2;
     using Red = float;
@@ -332,8 +408,8 @@ struct PolQ4_K {
     static constexpr int kConsWarps = 4;
     static constexpr int kConsWarpsFewAcc = 4;
     static constexpr bool kComputeBound = true;
-    static constexpr bool kRowSplit = false;
     static constexpr bool kColSplit = false;
+    static constexpr bool kRuntimeCols = false;     // consume_pair, see PolQ8_0Wide
     static constexpr bool kNibbles = true;
     using Acc = float2;
     using Red = float;
@@ -435,8 +511,8 @@ struct PolI8 {
     static constexpr int kConsWarps = 2;
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
-    static constexpr bool kRowSplit = false;
     static constexpr bool kColSplit = false;
+    static constexpr bool kRuntimeCols = false;     // consume_pair, see PolQ8_0Wide
     static constexpr bool kNibbles = false;
     using Acc = int;
     using Red = int;
@@ -468,23 +544,11 @@ struct PolI8 {
     __device__ __forceinline__ static Red finish(const Acc &a) { return a; }
 };
 
-// Row-split stages (three or more vectors, float formats).  A stage holds the
-// tile's rows for all CW consumer warps (CW x 32 rows) and one x tile; every
-// warp consumes every stage, each its own 32 rows, and the stage is free once
-// all CW warps have arrived.  The x tile of a K chunk is then loaded and held
-// once per CTA instead of once per warp, which at eight vectors is about half
-// of a warp's shared memory: more warps fit on an SM.  Each row has one owner,
-// so a tile needs no reduction across warps.  The decode must leave x as it
-// is (the decodes of three or more vectors do).
-template <class Base>
-struct PolRowSplit : Base {
-    static constexpr bool kRowSplit = true;
-};
-
 // Column-split stages (the 4-bit formats at one vector, whose decode sets the
-// pace).  As with row-split stages every consumer warp consumes every stage,
-// but each takes its own blocks of all the stage's rows; the tile's partial
-// sums are added across the warps at its end.  A stage is then in use for a
+// pace, and Q8_0 at three or more vectors).  Every consumer warp consumes
+// every stage, each its own blocks of all the stage's rows; the tile's partial
+// sums are added across the warps at its end.  The stage's x tile is loaded
+// once for all warps.  A stage is then in use for a
 // quarter of the time one warp would need for it, so the same shared memory
 // keeps more bytes in flight.
 template <class Base>
@@ -563,7 +627,7 @@ __host__ __device__ constexpr int cons_warps() { return (NV * R <= 2) ? P::kCons
 
 template <class P, int NV, int R, bool MOE>
 struct Layout {
-    static constexpr int TR = 32 * R * (P::kRowSplit ? cons_warps<P, NV, R>() : 1);   // rows per tile
+    static constexpr int TR = 32 * R;                                   // rows per tile
     static constexpr int WT = TR * P::kChunkBytes;                      // weight tile bytes
     static constexpr int kAlign = P::kSwizzle ? 1024 : 128;            // TMA destination alignment
     static constexpr int XT = ((NV * P::kChunkCols * P::kXElemBytes + kAlign - 1) / kAlign) * kAlign;
@@ -573,7 +637,7 @@ struct Layout {
     // s = ring stages, ks = CTAs per cluster along K (the gather buffer exists only when ks > 1)
     __host__ __device__ static size_t red_off(int s) { return (size_t)s * ST; }
     __host__ __device__ static size_t part_off(int s) {
-        return red_off(s) + (size_t)(P::kRowSplit ? 1 : cons_warps<P, NV, R>()) * TR * NV * 4;
+        return red_off(s) + (size_t)cons_warps<P, NV, R>() * TR * NV * 4;
     }
     __host__ __device__ static size_t bar_off(int s, int ks) {
         return part_off(s) + (ks > 1 ? (size_t)ks * TR * NV * 4 : 0);
@@ -654,11 +718,15 @@ template <class P, int NV, int R>
 __device__ __forceinline__ void consume_cols(const uint8_t *wt, const uint8_t *xt, int lane, int warp,
                                              typename P::Acc (&acc)[R][NV]) {
     static_assert(cons_warps<P, NV, R>() == 4 && P::kUnits == 8, "four warps of two units each");
-    switch (warp) {
-        case 0: P::template consume<NV, R, 0, 2>(wt, xt, lane, acc); break;
-        case 1: P::template consume<NV, R, 2, 2>(wt, xt, lane, acc); break;
-        case 2: P::template consume<NV, R, 4, 2>(wt, xt, lane, acc); break;
-        default: P::template consume<NV, R, 6, 2>(wt, xt, lane, acc); break;
+    if constexpr (P::kRuntimeCols) {
+        P::template consume_pair<NV, R>(wt, xt, lane, warp, acc);
+    } else {
+        switch (warp) {
+            case 0: P::template consume<NV, R, 0, 2>(wt, xt, lane, acc); break;
+            case 1: P::template consume<NV, R, 2, 2>(wt, xt, lane, acc); break;
+            case 2: P::template consume<NV, R, 4, 2>(wt, xt, lane, acc); break;
+            default: P::template consume<NV, R, 6, 2>(wt, xt, lane, acc); break;
+        }
     }
 }
 
@@ -676,9 +744,9 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 // owns the tile's 32*R rows (R per lane); S is a multiple of CW, so every
 // stage has one owner.  A tile ends with a fixed-order reduction over the CW
 // warps; with a K split, the CTAs of a cluster then combine their partials
-// through DSMEM.  With row-split stages (PolRowSplit) a tile is CW*32*R rows,
-// every warp consumes every fill (its own 32*R rows, one shared x tile), and
-// the stage is freed by all CW warps; rows need no reduction across warps.
+// through DSMEM.  With column-split stages (PolColSplit) every warp consumes
+// every fill (its own blocks of the tile's rows), and the stage is freed by
+// all CW warps.
 //
 // Programmatic dependent launch: the kernel lets the next one in the stream
 // start as soon as it is resident, issues the weight copies of its first
@@ -690,7 +758,8 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 // four or more consumer warps.
 template <class P, int NV, int R>
 constexpr int ctas_per_sm() {
-    if constexpr (P::kRowSplit) return NV <= 4 ? 5 : 4;
+    // Q8_0 at three or more vectors: 75-104 registers, three CTAs of four consumer warps
+    if constexpr (std::is_base_of<PolQ8_0Wide, P>::value) return 3;
     // Q4_0 at 2-6 vectors: its 96-116 registers leave room for a third CTA
     // (8B-shaped token n_vec 3 / 4: 1865 / 1606 -> 1939 / 1651 GB/s; n_vec 2,
     // with a ring of one stage per warp: 2520 -> 2733 GB/s)
@@ -727,14 +796,13 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nthreads = blockDim.x;
-    constexpr int CW = cons_warps<P, NV, R>();      // S % CW == 0 unless rows are split (see make_plan)
-    constexpr bool RS = P::kRowSplit;
-    constexpr bool SH = P::kRowSplit || P::kColSplit;   // every warp consumes every stage
+    constexpr int CW = cons_warps<P, NV, R>();      // S % CW == 0 unless columns are split (see make_plan)
+    constexpr bool SH = P::kColSplit;               // every warp consumes every stage
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
-            mbar_init(smem_u32(&empty[i]), SH ? CW : 1);   // row / column split: every warp frees the stage
+            mbar_init(smem_u32(&empty[i]), SH ? CW : 1);   // column split: every warp frees the stage
         }
         mbar_init(smem_u32(gather_bar), (uint32_t)max(a.ksplit - 1, 1));
         *abort_flag = 0;
@@ -897,8 +965,8 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
             // fill n lands in stage n % S and belongs to warp n % CW (S is a multiple
             // of CW): each stage is only ever consumed by one warp, in fill order,
             // so a wait can never mistake a stage's previous phase for its next.
-            // Row split: every warp consumes every fill (its own 32 * R rows of
-            // the stage), so each warp waits on every phase of every stage in order.
+            // Column split: every warp consumes every fill (its own blocks of the
+            // stage), so each warp waits on every phase of every stage in order.
             for (int j = SH ? 0 : (warp - (int)(base % CW) + CW) % CW; j < nloc; j += SH ? 1 : CW) {
                 const uint32_t n = base + j;
                 const int s = n % S;
@@ -906,7 +974,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 uint8_t *st = smem + (size_t)s * ST;
                 if constexpr (!MOE) {
                     if constexpr (P::kColSplit) consume_cols<P, NV, R>(st, st + WT, lane, warp, acc);
-                    else consume_chunk<P, NV, R>(st + (RS ? (size_t)warp * 32 * R * P::kChunkBytes : 0), st + WT, lane, acc);
+                    else consume_chunk<P, NV, R>(st, st + WT, lane, acc);
                 } else {
                     // only the group's m vectors are multiplied
                     switch (m) {
@@ -931,12 +999,11 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 if (lane == 0) mbar_arrive(smem_u32(&empty[s]));
             }
             // reduction of the tile over all consumer warps, in fixed warp order
-            // (row split: each row has one warp, which writes it in place)
 #pragma unroll
             for (int r = 0; r < R; ++r)
 #pragma unroll
                 for (int v = 0; v < NV; ++v)
-                    red[RS ? v * TR + warp * 32 * R + lane + 32 * r : (warp * NV + v) * TR + lane + 32 * r] =
+                    red[(warp * NV + v) * TR + lane + 32 * r] =
                         P::finish(acc[r][v]);
             named_barrier(1, CW * 32);
             if (gs) {
@@ -945,7 +1012,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
                 for (int rr = threadIdx.x; rr < TR; rr += CW * 32)
                     for (int v = 0; v < m; ++v) {
                         Red sum = red[v * TR + rr];
-                        for (int w2 = 1; w2 < (RS ? 1 : CW); ++w2) sum += red[(w2 * NV + v) * TR + rr];
+                        for (int w2 = 1; w2 < CW; ++w2) sum += red[(w2 * NV + v) * TR + rr];
                         const int p = mt.sorted[mt.gstart[g] + v];
                         float &c = csum[(p / a.n_active) * TR + rr];
                         c = fmaf(a.router_w[p], (float)sum, c);
@@ -954,7 +1021,7 @@ matvec_tma_kernel(const __grid_constant__ KArgs a) {
             for (int e = threadIdx.x; e < TR * m && !gs; e += CW * 32) {
                 const int v = e / TR, rr = e % TR;
                 Red sum = red[v * TR + rr];
-                for (int w2 = 1; w2 < (RS ? 1 : CW); ++w2) sum += red[(w2 * NV + v) * TR + rr];
+                for (int w2 = 1; w2 < CW; ++w2) sum += red[(w2 * NV + v) * TR + rr];
                 const long long row = (long long)tile * TR + rr;
                 if (split) {
                     // this CTA's partial goes to slot `rank` of the leader's gather buffer
@@ -1252,11 +1319,11 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     const int want = ctas_per_sm<P, NV, R>();
     constexpr int CW = cons_warps<P, NV, R>();
     // stages come in multiples of CW (one owner each), or of one when every warp
-    // consumes every stage (row split)
-    constexpr bool SH = P::kRowSplit || P::kColSplit;
+    // consumes every stage (column split)
+    constexpr bool SH = P::kColSplit;
     constexpr int SQ = SH ? 1 : CW;
     // two stages per consumer warp (a double buffer each), more when room allows;
-    // row split: two stages for the CTA, more when room allows
+    // column split: two stages for the CTA, more when room allows
     // Q4_0 at one vector starts from one stage per warp: with four consumer
     // warps the ring then leaves room for 3 CTAs per SM (2 with two stages per
     // warp); the ring still grows below when fewer CTAs are resident.  8B-shaped
@@ -1279,7 +1346,11 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     const long long slots = (long long)dev.num_sms * per_sm;
     int ks = 1;
     p.slots = slots;
-    while (gsplit == 0 && ks < kMaxSplit && n_work * ks * 2 <= slots && n_chunks >= 2 * ks) ks *= 2;
+    // (the wide-vector policy's gather buffer is large: a split must leave its CTAs per SM room)
+    constexpr bool kFitSplit = std::is_base_of<PolQ8_0Wide, P>::value;
+    while (gsplit == 0 && ks < kMaxSplit && n_work * ks * 2 <= slots && n_chunks >= 2 * ks &&
+           (!kFitSplit || L::total(2, 2 * ks) * per_sm <= budget))
+        ks *= 2;
     // Q4_0 (decode-bound) on launches short enough that the largest K split
     // that still fits one wave leaves each CTA at most three chunks: that split
     // fills every CTA slot (o 4096x4096: clusters of 7, 1626 -> 1880 GB/s; the
@@ -1432,10 +1503,10 @@ hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
     return HQ_OK;
 }
 
-// Rows per lane: two for Q4_0 at one or two vectors (the second row shares the
-// x loads and adds independent work to a warp whose decode, not HBM, is the
-// limit); one otherwise -- with three or more vectors a 64-row stage plus its
-// x tile leaves room for too few CTAs per SM.
+// Rows per lane: two for the 4-bit formats at one or two vectors (the second
+// row shares the x loads and adds independent work to a warp whose decode, not
+// HBM, is the limit); one otherwise (Q8_0 at three or more vectors takes two
+// in with_dense_policy).
 template <class P>
 constexpr int rows_per_lane(int nv) {
     return (P::kNibbles && nv <= 2) ? 2 : 1;
@@ -1499,12 +1570,13 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
     } else if constexpr (std::is_same<P, PolQ8_0>::value && NV == 2) {
         return f(PolQ8_0Two{}, RT{});
     } else if constexpr (std::is_same<P, PolQ8_0>::value) {
-        // Q8_0 at three or more vectors: row-split stages, one x tile per CTA
-        // (8B-shaped token at n_vec 3 / 4 / 6 / 8: 2674 / 2255 / 1654 / 1310 ->
-        // 3240 / 2730 / 1720 / 1328 GB/s; at n_vec 2 no gain).  Q4_0 keeps one
-        // owner per stage: with its 128-row split stages it measured 1866 / 1605 /
-        // 1007 -> 1794 / 1586 / 926 GB/s at n_vec 3 / 4 / 8.
-        return f(PolRowSplit<P>{}, RT{});
+        // Q8_0 at three or more vectors: column-split stages of 64-row tiles, two
+        // rows per lane, the scale folded into each weight (PolQ8_0Wide).  Against
+        // the row-split stages of one row per lane it replaced (one 32-row share
+        // of every stage per warp), the 8B-shaped token at n_vec 3 / 4 / 5 / 8:
+        // 3280 / 2716 / 2045 / 1335 -> 3605 / 2952 / 2764 / 2135 GB/s.  Three
+        // rows per lane (96-row tiles) lost on the K-split launches.
+        return f(PolColSplit<PolQ8_0Wide>{}, std::integral_constant<int, 2>{});
     } else if constexpr (P::kNibbles && (NV == 1 || (NV == 2 && std::is_same<P, PolQ4_0>::value))) {
         // column-split stages where the launch does not split K over clusters
         // (enough 64-row tiles to give every CTA slot two): Q4_0 gate|up
@@ -1536,7 +1608,7 @@ template <class Pol>
 constexpr int policy_id() {
     return std::is_same<Pol, PolQ8_0Short>::value ? 1
          : std::is_same<Pol, PolQ8_0Two>::value ? 2
-         : Pol::kRowSplit ? 3 : Pol::kColSplit ? 4 : 0;
+         : Pol::kColSplit ? 4 : 0;
 }
 
 // Test-only: the geometry make_plan gives one dense launch, for a device
