@@ -384,6 +384,104 @@ struct PolQ4_0 {
     __device__ __forceinline__ static Red finish(const Acc &a) { return a.x + a.y; }
 };
 
+// Q4_0 at three or more vectors: as PolQ8_0Wide, two rows per lane and the
+// block scale folded into each weight.  A nibble n masked in place at bit p
+// and ORed into 2^23 is f = 2^23 + n 2^p; with d_p = d 2^-p one packed fma
+// gives f d_p - (2^23 + 8 2^p) d_p = (n - 8) d exactly when (2^(23-p) + 8) d
+// is representable, i.e. for p >= 8 inside the mantissa: p = 8, 12 and 16
+// ((2^12 + 1), (2^8 + 1) and 17 times 2^3 d: 13, 9 and 5 significant bits
+// times d's 11).  Of a word's four quant bytes, byte 1 lies at bits 8..15 and
+// byte 2 at 16..23 as loaded; one prmt brings bytes 0 and 3 there, and two
+// shifts bring the high nibbles of bytes 2 and 3 to bit 12.  Each packed pair
+// then shares one p.
+struct PolQ4_0Wide : PolQ4_0 {
+    static constexpr bool kRuntimeCols = true;      // see consume_pair
+
+    // Blocks 2p and 2p + 1 of the stage's chunk: 36 bytes from byte 36p of each
+    // row chunk, 9 words from a 4-byte-aligned start (block 0: d in word 0's
+    // low half, quant bytes from byte 2; block 1: d in word 4's high half,
+    // quant bytes in words 5..8).
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume_pair(const uint8_t *__restrict__ wt,
+                                                        const uint8_t *__restrict__ xt8, int lane, int p,
+                                                        Acc (&acc)[R][NV]) {
+        const float *xt = reinterpret_cast<const float *>(xt8) + 64 * p;
+        const uint32_t magic = opaque_magic();
+        uint32_t w[R][9];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t *rp = reinterpret_cast<const uint32_t *>(wt + (lane + 32 * r) * kChunkBytes + 36 * p);
+#pragma unroll
+            for (int k = 0; k < 9; ++k) w[r][k] = rp[k];
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float2 d8[R], c8[R], d12[R], c12[R], d16[R], c16[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const unsigned short hb = h ? (unsigned short)(w[r][4] >> 16) : (unsigned short)(w[r][0] & 0xffffu);
+                const float d = __half2float(__ushort_as_half(hb));
+                const float e8 = d * 0.00390625f, e12 = d * 0.000244140625f, e16 = d * 0.0000152587890625f;
+                d8[r] = make_float2(e8, e8);
+                d12[r] = make_float2(e12, e12);
+                d16[r] = make_float2(e16, e16);
+                const float k8 = -8390656.0f * e8, k12 = -8421376.0f * e12, k16 = -8912896.0f * e16;
+                c8[r] = make_float2(k8, k8);        // -(2^23 + 2^11) d / 2^8
+                c12[r] = make_float2(k12, k12);     // -(2^23 + 2^15) d / 2^12
+                c16[r] = make_float2(k16, k16);     // -(2^23 + 2^19) d / 2^16
+            }
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                // quant bytes 4k..4k+3 of block h: low nibbles are q_{4k..4k+3},
+                // high nibbles q_{16+4k..16+4k+3}
+                uint32_t gw[R], gb[R];
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    gw[r] = h ? w[r][5 + k] : __funnelshift_r(w[r][k], w[r][k + 1], 16);
+                    gb[r] = prmt(gw[r], 0u, 0x0300u);      // byte 0 at bits 8..15, byte 3 at 16..23
+                }
+                {
+                    float4 xv[NV];
+#pragma unroll
+                    for (int v = 0; v < NV; ++v)
+                        xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * h + 4 * k);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float2 w01 = ffma2(make_float2(nib<0xF00u>(gb[r], magic), nib<0xF00u>(gw[r], magic)),
+                                                 d8[r], c8[r]);
+                        const float2 w23 = ffma2(make_float2(nib<0xF0000u>(gw[r], magic), nib<0xF0000u>(gb[r], magic)),
+                                                 d16[r], c16[r]);
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) {
+                            acc[r][v] = ffma2(w01, make_float2(xv[v].x, xv[v].y), acc[r][v]);
+                            acc[r][v] = ffma2(w23, make_float2(xv[v].z, xv[v].w), acc[r][v]);
+                        }
+                    }
+                }
+                {
+                    float4 xv[NV];
+#pragma unroll
+                    for (int v = 0; v < NV; ++v)
+                        xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * h + 16 + 4 * k);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+                        const float2 w01 = ffma2(make_float2(nib<0xF000u>(gb[r], magic), nib<0xF000u>(gw[r], magic)),
+                                                 d12[r], c12[r]);
+                        const float2 w23 = ffma2(make_float2(nib<0xF000u>(gw[r] >> 8, magic),
+                                                             nib<0xF000u>(gw[r] >> 16, magic)),
+                                                 d12[r], c12[r]);
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) {
+                            acc[r][v] = ffma2(w01, make_float2(xv[v].x, xv[v].y), acc[r][v]);
+                            acc[r][v] = ffma2(w23, make_float2(xv[v].z, xv[v].w), acc[r][v]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+};
+
 // Q4_K ("One Native Stack ...", sections "The Unified Quant Core" and "Ported
 // Versus Novel": ggml's super-block of 256 weights in 144 B).  A 256-column
 // chunk of a row is exactly one super-block: 16-byte unit 0 holds fp16 d,
@@ -501,6 +599,82 @@ struct PolQ4_K {
     __device__ __forceinline__ static Red finish(const Acc &a) { return a.x + a.y; }
 };
 
+// Q4_K at three or more vectors: two rows per lane, column-split stages, and
+// one copy of the decode for all four warps: warp p takes quant group p
+// (sub-blocks 2p and 2p + 1) with p in a register, and reads the two
+// sub-blocks' six-bit scales and mins with run-time shifts.  The weights are
+// formed as in PolQ4_K.
+struct PolQ4_KWide : PolQ4_K {
+    static constexpr bool kRuntimeCols = true;      // see consume_pair
+
+    __device__ __forceinline__ static uint32_t six_rt(int j, int sel, uint32_t s0, uint32_t s1, uint32_t s2) {
+        const uint32_t sm = sel ? s1 : s0;
+        if (j < 4) return (sm >> (8 * j)) & 63u;
+        const uint32_t lo4 = (s2 >> (8 * (j - 4) + 4 * sel)) & 15u;
+        const uint32_t hi2 = (sm >> (8 * (j - 4) + 6)) & 3u;
+        return lo4 | (hi2 << 4);
+    }
+
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume_pair(const uint8_t *__restrict__ wt,
+                                                        const uint8_t *__restrict__ xt8, int lane, int p,
+                                                        Acc (&acc)[R][NV]) {
+        const float *xt = reinterpret_cast<const float *>(xt8) + 64 * p;
+        const float2 kM = make_float2(-8388608.0f, -8388608.0f);          // -2^23
+        const uint32_t magic = opaque_magic();
+        float2 alo[R], ahi[R], blo[R], bhi[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint4 hdr = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes)[0];
+            const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
+            const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+            const float a0 = d * (float)six_rt(2 * p, 0, hdr.y, hdr.z, hdr.w);
+            const float a1 = d * (float)six_rt(2 * p + 1, 0, hdr.y, hdr.z, hdr.w);
+            const float b0 = dm * (float)six_rt(2 * p, 1, hdr.y, hdr.z, hdr.w);
+            const float b1 = dm * (float)six_rt(2 * p + 1, 1, hdr.y, hdr.z, hdr.w);
+            alo[r] = make_float2(a0, a0 * 0.00390625f);                  // nibbles at bits 0 and 8
+            ahi[r] = make_float2(a1 * 0.0625f, a1 * 0.000244140625f);     // nibbles at bits 4 and 12
+            blo[r] = make_float2(-b0, -b0);
+            bhi[r] = make_float2(-b1, -b1);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {                   // the group's two 16-byte units
+            uint32_t qw[R][4];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint4 q = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes)[1 + 2 * p + u];
+                qw[r][0] = q.x; qw[r][1] = q.y; qw[r][2] = q.z; qw[r][3] = q.w;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {            // quant bytes 4k .. 4k+3 of the group
+                const int k = 4 * u + kk;
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi) {        // sub-block 2p (low nibbles), then 2p + 1
+                    float4 xv[NV];
+#pragma unroll
+                    for (int v = 0; v < NV; ++v)
+                        xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * hi + 4 * k);
+#pragma unroll
+                    for (int r = 0; r < R; ++r) {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint32_t w = h ? (qw[r][kk] >> 16) : qw[r][kk];
+                            const float2 q = hi ? fadd2(make_float2(nib<0xF0u>(w, magic), nib<0xF000u>(w, magic)), kM)
+                                                : fadd2(make_float2(nib<0xFu>(w, magic), nib<0xF00u>(w, magic)), kM);
+                            const float2 wq = hi ? ffma2(ahi[r], q, bhi[r]) : ffma2(alo[r], q, blo[r]);
+#pragma unroll
+                            for (int v = 0; v < NV; ++v) {
+                                const float2 xp = h ? make_float2(xv[v].z, xv[v].w) : make_float2(xv[v].x, xv[v].y);
+                                acc[r][v] = ffma2(wq, xp, acc[r][v]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+};
+
 struct PolI8 {
     static constexpr int kChunkCols = 128;          // one 128-byte swizzle span
     static constexpr int kChunkBytes = 128;
@@ -545,7 +719,8 @@ struct PolI8 {
 };
 
 // Column-split stages (the 4-bit formats at one vector, whose decode sets the
-// pace, and Q8_0 at three or more vectors).  Every consumer warp consumes
+// pace; Q8_0 at three or more vectors and the 4-bit formats at four or more,
+// where the FP32 pipe does).  Every consumer warp consumes
 // every stage, each its own blocks of all the stage's rows; the tile's partial
 // sums are added across the warps at its end.  The stage's x tile is loaded
 // once for all warps.  A stage is then in use for a
@@ -759,7 +934,9 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 template <class P, int NV, int R>
 constexpr int ctas_per_sm() {
     // Q8_0 at three or more vectors: 75-104 registers, three CTAs of four consumer warps
-    if constexpr (std::is_base_of<PolQ8_0Wide, P>::value) return 3;
+    if constexpr (std::is_base_of<PolQ8_0Wide, P>::value || std::is_base_of<PolQ4_0Wide, P>::value ||
+                  std::is_base_of<PolQ4_KWide, P>::value)
+        return 3;
     // Q4_0 at 2-6 vectors: its 96-116 registers leave room for a third CTA
     // (8B-shaped token n_vec 3 / 4: 1865 / 1606 -> 1939 / 1651 GB/s; n_vec 2,
     // with a ring of one stage per warp: 2520 -> 2733 GB/s)
@@ -1347,7 +1524,8 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     int ks = 1;
     p.slots = slots;
     // (the wide-vector policy's gather buffer is large: a split must leave its CTAs per SM room)
-    constexpr bool kFitSplit = std::is_base_of<PolQ8_0Wide, P>::value;
+    constexpr bool kFitSplit = std::is_base_of<PolQ8_0Wide, P>::value || std::is_base_of<PolQ4_0Wide, P>::value ||
+                               std::is_base_of<PolQ4_KWide, P>::value;
     while (gsplit == 0 && ks < kMaxSplit && n_work * ks * 2 <= slots && n_chunks >= 2 * ks &&
            (!kFitSplit || L::total(2, 2 * ks) * per_sm <= budget))
         ks *= 2;
@@ -1505,8 +1683,8 @@ hq_status launch_tma(KArgs &a, const Plan &p, cudaStream_t stream) {
 
 // Rows per lane: two for the 4-bit formats at one or two vectors (the second
 // row shares the x loads and adds independent work to a warp whose decode, not
-// HBM, is the limit); one otherwise (Q8_0 at three or more vectors takes two
-// in with_dense_policy).
+// HBM, is the limit); one otherwise (the wide-vector policies chosen in
+// with_dense_policy take two).
 template <class P>
 constexpr int rows_per_lane(int nv) {
     return (P::kNibbles && nv <= 2) ? 2 : 1;
@@ -1577,6 +1755,15 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
         // 3280 / 2716 / 2045 / 1335 -> 3605 / 2952 / 2764 / 2135 GB/s.  Three
         // rows per lane (96-row tiles) lost on the K-split launches.
         return f(PolColSplit<PolQ8_0Wide>{}, std::integral_constant<int, 2>{});
+    } else if constexpr (std::is_same<P, PolQ4_0>::value && NV >= 4) {
+        // the 4-bit formats from four vectors on, where the FP32 pipe binds: as
+        // Q8_0 above (Q4_0 token n_vec 4 / 6 / 8: 1658 / 1284 / 1008 -> 1681 /
+        // 1326 / 1131 GB/s; at n_vec 3 it lost, 1930 -> 1730)
+        return f(PolColSplit<PolQ4_0Wide>{}, std::integral_constant<int, 2>{});
+    } else if constexpr (std::is_same<P, PolQ4_K>::value && NV >= 4) {
+        // (Q4_K token n_vec 4 / 6 / 8: 1521 / 1192 / 953 -> 1569 / 1247 / 1075
+        // GB/s; at n_vec 3 it lost, 1752 -> 1682)
+        return f(PolColSplit<PolQ4_KWide>{}, std::integral_constant<int, 2>{});
     } else if constexpr (P::kNibbles && (NV == 1 || (NV == 2 && std::is_same<P, PolQ4_0>::value))) {
         // column-split stages where the launch does not split K over clusters
         // (enough 64-row tiles to give every CTA slot two): Q4_0 gate|up

@@ -77,6 +77,8 @@ def expected_policy(fmt, n_vec, rows, cols):
         return 2
     if fmt == 8:
         return 4                # column-split stages, two rows per lane
+    if fmt in (4, 75) and n_vec >= 4:
+        return 4                # column-split stages, two rows per lane
     if (fmt in (4, 75) and n_vec == 1) or (fmt == 4 and n_vec == 2):
         # column-split stages unless K is split over clusters (64-row tiles too
         # few to give each of the 152 x 3 CTA slots two)
@@ -97,7 +99,7 @@ def test_plan_invariants(hq, fmt):
         what = f"fmt {fmt} {rows}x{cols} n_vec={n_vec}: {p}"
         n_chunks = cols // chunk
         assert p["policy"] == expected_policy(fmt, n_vec, rows, cols), what
-        rpl = 2 if (fmt in (4, 75) and n_vec <= 2) or (fmt == 8 and n_vec >= 3) else 1
+        rpl = 2 if (fmt in (4, 75) and n_vec != 3) or (fmt == 8 and n_vec >= 3) else 1
         assert p["tile_rows"] == 32 * rpl, what
         assert p["tiles"] == math.ceil(rows / p["tile_rows"]), what
         # the ring: one owner per stage (a multiple of the consumer warps), or at
