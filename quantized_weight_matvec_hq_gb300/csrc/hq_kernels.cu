@@ -86,7 +86,7 @@ struct PolQ8_0 {
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
     static constexpr bool kColSplit = false;        // see PolColSplit
-    static constexpr bool kRuntimeCols = false;     // consume_pair, see PolQ8_0Wide
+    static constexpr bool kRuntimeCols = false;     // column-split decode at a run-time offset (consume_pair)
     static constexpr bool kNibbles = false;         // 4-bit quants (decode-bound launch policies)
     using Acc = float2;
     using Red = float;
@@ -306,7 +306,7 @@ struct PolQ4_0 {
     static constexpr int kConsWarpsFewAcc = 4;      // n_vec 1 (two rows per lane; see make_plan's ring)
     static constexpr bool kComputeBound = true;     // decode, not HBM, sets the pace
     static constexpr bool kColSplit = false;
-    static constexpr bool kRuntimeCols = false;     // consume_pair, see PolQ8_0Wide
+    static constexpr bool kRuntimeCols = false;     // column-split decode at a run-time offset (consume_pair)
     static constexpr bool kNibbles = true;
     using Acc = float2;
     using Red = float;
@@ -382,6 +382,75 @@ struct PolQ4_0 {
         }
     }
     __device__ __forceinline__ static Red finish(const Acc &a) { return a.x + a.y; }
+};
+
+// Q4_0 at one or two vectors with column-split stages: the decode of PolQ4_0
+// on a pair of blocks at a run-time offset, so that one copy of it serves all
+// four warps.  Blocks 2p and 2p + 1 are 36 bytes from byte 36p of each row
+// chunk: 9 words from a 4-byte-aligned start, the same positions for every p.
+struct PolQ4_0Pair : PolQ4_0 {
+    static constexpr bool kRuntimeCols = true;
+
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume_pair(const uint8_t *__restrict__ wt,
+                                                        const uint8_t *__restrict__ xt8, int lane, int p,
+                                                        Acc (&acc)[R][NV]) {
+        const float *xt = reinterpret_cast<const float *>(xt8) + 64 * p;
+        const float2 kBiasLo = make_float2(-8388616.0f, -8390656.0f);   // -(2^23 + 8), -(2^23 + 8 * 2^8)
+        const float2 kBiasHi = make_float2(-8388736.0f, -8421376.0f);   // -(2^23 + 8 * 2^4), -(2^23 + 8 * 2^12)
+        const float2 kSixteenth = make_float2(0.0625f, 0.0625f);
+        const uint32_t magic = opaque_magic();
+        uint32_t w[R][9];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t *rp = reinterpret_cast<const uint32_t *>(wt + (lane + 32 * r) * kChunkBytes + 36 * p);
+#pragma unroll
+            for (int k = 0; k < 9; ++k) w[r][k] = rp[k];
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            float2 slo[R][NV], shi[R][NV];
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int v = 0; v < NV; ++v) slo[r][v] = shi[r][v] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+                float4 xv[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * h + 4 * g);
+                const bool high = g >= 4;
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int t = (4 * g + 2 * e) & 15;
+                        const int o = 18 * h + 2 + t;              // pair byte of quant bytes t, t + 1
+                        const uint32_t wd = (o & 2) ? (w[r][o >> 2] >> 16) : w[r][o >> 2];
+                        const float2 q = high
+                            ? fadd2(make_float2(nib<0xF0u>(wd, magic), nib<0xF000u>(wd, magic)), kBiasHi)
+                            : fadd2(make_float2(nib<0xFu>(wd, magic), nib<0xF00u>(wd, magic)), kBiasLo);
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) {
+                            const float2 xp = e ? make_float2(xv[v].z, xv[v].w) : make_float2(xv[v].x, xv[v].y);
+                            float2 &sv = high ? shi[r][v] : slo[r][v];
+                            sv = ffma2(q, xp, sv);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const unsigned short hb = h ? (unsigned short)(w[r][4] >> 16) : (unsigned short)(w[r][0] & 0xffffu);
+                const float d = __half2float(__ushort_as_half(hb));
+                const float2 dd = make_float2(d, d * 0.00390625f);          // bits 8/12 carry 2^8 more
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    acc[r][v] = ffma2(dd, ffma2(shi[r][v], kSixteenth, slo[r][v]), acc[r][v]);
+            }
+        }
+    }
 };
 
 // Q4_0 at three or more vectors: as PolQ8_0Wide, two rows per lane and the
@@ -507,7 +576,7 @@ struct PolQ4_K {
     static constexpr int kConsWarpsFewAcc = 4;
     static constexpr bool kComputeBound = true;
     static constexpr bool kColSplit = false;
-    static constexpr bool kRuntimeCols = false;     // consume_pair, see PolQ8_0Wide
+    static constexpr bool kRuntimeCols = false;     // column-split decode at a run-time offset (consume_pair)
     static constexpr bool kNibbles = true;
     using Acc = float2;
     using Red = float;
@@ -599,8 +668,8 @@ struct PolQ4_K {
     __device__ __forceinline__ static Red finish(const Acc &a) { return a.x + a.y; }
 };
 
-// Q4_K at three or more vectors: two rows per lane, column-split stages, and
-// one copy of the decode for all four warps: warp p takes quant group p
+// Q4_K with column-split stages (one vector, and four or more at two rows per
+// lane): one copy of the decode for all four warps: warp p takes quant group p
 // (sub-blocks 2p and 2p + 1) with p in a register, and reads the two
 // sub-blocks' six-bit scales and mins with run-time shifts.  The weights are
 // formed as in PolQ4_K.
@@ -637,6 +706,14 @@ struct PolQ4_KWide : PolQ4_K {
             blo[r] = make_float2(-b0, -b0);
             bhi[r] = make_float2(-b1, -b1);
         }
+        // with few accumulators the second sub-block's products go to a second set
+        // (two independent FMA chains per output)
+        constexpr bool kTwo = NV * R <= 2;
+        float2 acc2[R][NV];
+#pragma unroll
+        for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int v = 0; v < NV; ++v) acc2[r][v] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int u = 0; u < 2; ++u) {                   // the group's two 16-byte units
             uint32_t qw[R][4];
@@ -665,12 +742,19 @@ struct PolQ4_KWide : PolQ4_K {
 #pragma unroll
                             for (int v = 0; v < NV; ++v) {
                                 const float2 xp = h ? make_float2(xv[v].z, xv[v].w) : make_float2(xv[v].x, xv[v].y);
-                                acc[r][v] = ffma2(wq, xp, acc[r][v]);
+                                float2 &av = (kTwo && hi) ? acc2[r][v] : acc[r][v];
+                                av = ffma2(wq, xp, av);
                             }
                         }
                     }
                 }
             }
+        }
+        if constexpr (kTwo) {
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+                for (int v = 0; v < NV; ++v) acc[r][v] = fadd2(acc[r][v], acc2[r][v]);
         }
     }
 };
@@ -686,7 +770,7 @@ struct PolI8 {
     static constexpr int kConsWarpsFewAcc = 2;
     static constexpr bool kComputeBound = false;
     static constexpr bool kColSplit = false;
-    static constexpr bool kRuntimeCols = false;     // consume_pair, see PolQ8_0Wide
+    static constexpr bool kRuntimeCols = false;     // column-split decode at a run-time offset (consume_pair)
     static constexpr bool kNibbles = false;
     using Acc = int;
     using Red = int;
@@ -888,21 +972,14 @@ __device__ __forceinline__ void consume_chunk(const uint8_t *wt, const uint8_t *
     P::template consume<NV, R, 6, 2>(wt, xt, lane, acc);
 }
 
-// Column split: warp w of four consumes units [2w, 2w + 2) of every stage.
+// Column split: warp w of four consumes blocks (units) 2w and 2w + 1 of every
+// stage, with w a run-time value (one copy of the decode for all four warps).
 template <class P, int NV, int R>
 __device__ __forceinline__ void consume_cols(const uint8_t *wt, const uint8_t *xt, int lane, int warp,
                                              typename P::Acc (&acc)[R][NV]) {
-    static_assert(cons_warps<P, NV, R>() == 4 && P::kUnits == 8, "four warps of two units each");
-    if constexpr (P::kRuntimeCols) {
-        P::template consume_pair<NV, R>(wt, xt, lane, warp, acc);
-    } else {
-        switch (warp) {
-            case 0: P::template consume<NV, R, 0, 2>(wt, xt, lane, acc); break;
-            case 1: P::template consume<NV, R, 2, 2>(wt, xt, lane, acc); break;
-            case 2: P::template consume<NV, R, 4, 2>(wt, xt, lane, acc); break;
-            default: P::template consume<NV, R, 6, 2>(wt, xt, lane, acc); break;
-        }
-    }
+    static_assert(cons_warps<P, NV, R>() == 4 && P::kUnits == 8 && P::kRuntimeCols,
+                  "four warps of two units each, decoded at a run-time offset");
+    P::template consume_pair<NV, R>(wt, xt, lane, warp, acc);
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -1773,7 +1850,20 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
         // (1995 -> 1885), whose decode holds more registers per row.
         constexpr int TR = 32 * R;
         const bool k_split = (rows + TR - 1) / TR * 2 <= (long long)dev.num_sms * ctas_per_sm<P, NV, R>();
-        if (!k_split) return f(PolColSplit<P>{}, RT{});
+        // The column-split decode takes the warp's pair of blocks at a run-time
+        // offset (PolQ4_0Pair, PolQ4_KWide): one copy of it for the four warps
+        // instead of four with constant offsets, which the instruction cache
+        // held poorly (Q4_0 token 3060 -> 3161 GB/s, gate|up 3652 -> 3813, at
+        // two vectors 2320 -> 2399; Q4_K token 2551 -> 2572).  The same change
+        // on the Q8_0 one-vector decode lost (8B token 4955 -> 4048 GB/s): its
+        // 17 word loads per pair and the rolled loop cost more than the cache,
+        // and so did a rolled loop over the pair decodes on the 4-bit formats'
+        // K-split launches (Q4_0 token 3149 -> 3092, Q4_K 2572 -> 2497).  A
+        // fourth CTA per SM at 72 registers did not change the Q4_0 token.
+        if (!k_split) {
+            if constexpr (std::is_same<P, PolQ4_0>::value) return f(PolColSplit<PolQ4_0Pair>{}, RT{});
+            else return f(PolColSplit<PolQ4_KWide>{}, RT{});
+        }
         return f(P{}, RT{});
     } else {
         return f(P{}, RT{});

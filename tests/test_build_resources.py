@@ -38,8 +38,8 @@ RECORDED = [
     ("INS_7PolQ8_0ELi1ELi1ELb0E", 8, 1, 28672, 4096, 448, 58880),
     ("INS_12PolQ8_0ShortELi1ELi1ELb0E", 8, 1, 6144, 1024, 192, 39648),
     ("INS_11PolColSplitINS_11PolQ8_0WideEEELi8ELi2ELb0E", 8, 8, 28672, 4096, 448, 59584),
-    ("INS_11PolColSplitINS_7PolQ4_0EEELi1ELi2ELb0E", 4, 1, 28672, 4096, 448, 72976),
-    ("INS_11PolColSplitINS_7PolQ4_KEEELi1ELi2ELb0E", 75, 1, 28672, 4096, 448, 72976),
+    ("INS_11PolColSplitINS_11PolQ4_0PairEEELi1ELi2ELb0E", 4, 1, 28672, 4096, 448, 72976),
+    ("INS_11PolColSplitINS_11PolQ4_KWideEEELi1ELi2ELb0E", 75, 1, 28672, 4096, 448, 72976),
 ]
 
 

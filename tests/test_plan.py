@@ -49,8 +49,8 @@ PINS = [
     ((8, 1, 1024, 3072, 78), (256, 160, 8, None)),       # Qwen3-0.6B down
     ((8, 1, 151936, 1024, 78), (297, 160, 1, None)),     # Qwen3-0.6B lm_head
     ((8, 8, 28672, 4096, 104), (448, 160, 1, 59584)),    # Q8_0 n_vec 8, column-split stages (full capture)
-    ((4, 1, 28672, 4096, 88), (448, 160, 1, 72976)),     # Q4_0 gate|up, column-split stages (full capture)
-    ((75, 1, 28672, 4096, 121), (448, 160, 1, 72976)),   # Q4_K gate|up, column-split stages (full capture)
+    ((4, 1, 28672, 4096, 72), (448, 160, 1, 72976)),     # Q4_0 gate|up, column-split stages (full capture)
+    ((75, 1, 28672, 4096, 120), (448, 160, 1, 72976)),   # Q4_K gate|up, column-split stages (full capture)
     ((8, 1, 4096, 4096, 80), (512, 96, 4, 39904)),       # Q8_0 o (full capture)
     ((4, 1, 4096, 14336, 97), (256, 160, 4, None)),
     ((4, 1, 6144, 4096, 97), (384, 160, 4, None)),
