@@ -1847,7 +1847,10 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
         // 28672x4096 3386 -> 3635 GB/s; with a K split they lost (o 4096x4096
         // 1622 -> 1482, down 4096x14336 2877 -> 2413 GB/s).  At two vectors
         // the Q4_0 token gained (2137 -> 2277 GB/s) and the Q4_K token lost
-        // (1995 -> 1885), whose decode holds more registers per row.
+        // (1995 -> 1885), whose decode holds more registers per row.  With the
+        // run-time pair offset below, column split on the K-split launches
+        // still lost (Q4_0 token 3157 -> 2715, Q4_K 2572 -> 2397, Q4_0 at
+        // two vectors 2398 -> 2289).
         constexpr int TR = 32 * R;
         const bool k_split = (rows + TR - 1) / TR * 2 <= (long long)dev.num_sms * ctas_per_sm<P, NV, R>();
         // The column-split decode takes the warp's pair of blocks at a run-time
