@@ -270,6 +270,71 @@ struct PolQ8_0Wide : PolQ8_0 {
     }
 };
 
+// Q8_0 at three or more vectors on launches that split K over clusters: eight
+// consumer warps, each one block of every stage, so that the launch's few CTAs
+// (1.7 per SM on the 8B-shaped o, q|k|v and down) bring twice the warps.
+struct PolQ8_0Wide8 : PolQ8_0Wide {
+    static constexpr int kConsWarps = 8;
+    static constexpr int kConsWarpsFewAcc = 8;
+
+    // block 2p + H of the chunk: words 8H .. 8H + 8 of the pair at byte 68p
+    // (block 0: d in word 0's low half, quant bytes 2..33; block 1: d in word
+    // 8's high half, quant bytes in words 9..16)
+    template <int NV, int R, int H>
+    __device__ __forceinline__ static void consume_half(const uint8_t *__restrict__ wt,
+                                                        const uint8_t *__restrict__ xt8, int lane, int p,
+                                                        Acc (&acc)[R][NV]) {
+        const float *xt = reinterpret_cast<const float *>(xt8) + 64 * p + 32 * H;
+        uint32_t w[R][9];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t *rp =
+                reinterpret_cast<const uint32_t *>(wt + (lane + 32 * r) * kChunkBytes + 68 * p) + 8 * H;
+#pragma unroll
+            for (int k = 0; k < 9; ++k) w[r][k] = rp[k] ^ 0x80808080u;
+        }
+        float2 dd[R], cc[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const unsigned short hb = (unsigned short)((H ? (w[r][0] >> 16) : (w[r][0] & 0xffffu)) ^ 0x8080u);
+            const float dq = __half2float(__ushort_as_half(hb)) * 0.00390625f;
+            const float c = -8421376.0f * dq;
+            dd[r] = make_float2(dq, dq);
+            cc[r] = make_float2(c, c);
+        }
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+            float4 xv[NV];
+#pragma unroll
+            for (int v = 0; v < NV; ++v)
+                xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 4 * g);
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float f[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int o = 2 * H + 2 + 4 * g + i;          // byte of quant 4g+i from word 8H
+                    f[i] = byte_mid_as_float(w[r][o >> 2], o & 3);
+                }
+                const float2 w01 = ffma2(make_float2(f[0], f[1]), dd[r], cc[r]);
+                const float2 w23 = ffma2(make_float2(f[2], f[3]), dd[r], cc[r]);
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    acc[r][v] = ffma2(w01, make_float2(xv[v].x, xv[v].y), acc[r][v]);
+                    acc[r][v] = ffma2(w23, make_float2(xv[v].z, xv[v].w), acc[r][v]);
+                }
+            }
+        }
+    }
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume_one(const uint8_t *__restrict__ wt,
+                                                       const uint8_t *__restrict__ xt8, int lane, int b,
+                                                       Acc (&acc)[R][NV]) {
+        if (b & 1) consume_half<NV, R, 1>(wt, xt8, lane, b >> 1, acc);
+        else consume_half<NV, R, 0>(wt, xt8, lane, b >> 1, acc);
+    }
+};
+
 // Q4_0 nibble decode, one and-or per element: a nibble at bit p in {0, 4, 8,
 // 12}, masked in place and ORed into the exponent of 2^23, is the fp32 value
 // 2^23 + n * 2^p (exact: the mantissa has 23 bits); adding -(2^23 + 8 * 2^p)
@@ -977,9 +1042,11 @@ __device__ __forceinline__ void consume_chunk(const uint8_t *wt, const uint8_t *
 template <class P, int NV, int R>
 __device__ __forceinline__ void consume_cols(const uint8_t *wt, const uint8_t *xt, int lane, int warp,
                                              typename P::Acc (&acc)[R][NV]) {
-    static_assert(cons_warps<P, NV, R>() == 4 && P::kUnits == 8 && P::kRuntimeCols,
-                  "four warps of two units each, decoded at a run-time offset");
-    P::template consume_pair<NV, R>(wt, xt, lane, warp, acc);
+    constexpr int CW = cons_warps<P, NV, R>();
+    static_assert((CW == 4 || CW == 8) && P::kUnits == 8 && P::kRuntimeCols,
+                  "four warps of two units each (or eight of one), decoded at a run-time offset");
+    if constexpr (CW == 8) P::template consume_one<NV, R>(wt, xt, lane, warp, acc);
+    else P::template consume_pair<NV, R>(wt, xt, lane, warp, acc);
 }
 
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
@@ -1011,6 +1078,7 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 template <class P, int NV, int R>
 constexpr int ctas_per_sm() {
     // Q8_0 at three or more vectors: 75-104 registers, three CTAs of four consumer warps
+    if constexpr (std::is_base_of<PolQ8_0Wide8, P>::value) return 2;
     if constexpr (std::is_base_of<PolQ8_0Wide, P>::value || std::is_base_of<PolQ4_0Wide, P>::value ||
                   std::is_base_of<PolQ4_KWide, P>::value)
         return 3;
@@ -1831,6 +1899,20 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
         // of every stage per warp), the 8B-shaped token at n_vec 3 / 4 / 5 / 8:
         // 3280 / 2716 / 2045 / 1335 -> 3605 / 2952 / 2764 / 2135 GB/s.  Three
         // rows per lane (96-row tiles) lost on the K-split launches.
+        // Eight consumer warps, one block each (PolQ8_0Wide8), on launches that
+        // split K and keep the same split with them (the launch's CTAs then bring
+        // twice the warps): rows of at most 3072 columns at every n_vec
+        // (Qwen3-0.6B-shaped token at n_vec 3 / 4 / 8: 1101 / 996 / 764 -> 1261 /
+        // 1195 / 893 GB/s) and the longer rows at n_vec <= 4 (8B-shaped token at
+        // n_vec 4: 2945 -> 3149; at 5 / 6 / 8 it lost 1-2 %, at 3 it tied).
+        if (cols <= kShortRowCols || NV <= 4) {
+            const long long tiles = (rows + 63) / 64;
+            const int chunks = (int)(cols / PolQ8_0::kChunkCols);
+            const Plan p4 = make_plan<PolColSplit<PolQ8_0Wide>, NV, 2, false>(dev, tiles, chunks, 0);
+            const Plan p8 = make_plan<PolColSplit<PolQ8_0Wide8>, NV, 2, false>(dev, tiles, chunks, 0);
+            if (p4.ksplit > 1 && p8.ksplit >= p4.ksplit)
+                return f(PolColSplit<PolQ8_0Wide8>{}, std::integral_constant<int, 2>{});
+        }
         return f(PolColSplit<PolQ8_0Wide>{}, std::integral_constant<int, 2>{});
     } else if constexpr (std::is_same<P, PolQ4_0>::value && NV >= 4) {
         // the 4-bit formats from four vectors on, where the FP32 pipe binds: as

@@ -455,11 +455,15 @@ def test_moe_invalid_id_sets_fault_and_nan(hq, flags):
     (4100, 4096, 3),    # column-split stages (64-row tiles, two rows per lane), ragged last tile
     (4100, 4096, 6),
     (333, 14336, 7),    # column-split stages with a K split over a cluster
+    (4100, 4096, 3),    # eight consumer warps of one block each (K split kept), ragged last tile
+    (1000, 2048, 5),    # eight warps on short rows, clusters of 8
+    (300, 14336, 4),    # eight warps, clusters of 8 over long rows, ragged last tile
+    (1024, 3072, 8),    # eight warps at eight vectors (short rows)
 ])
 def test_q8_0_launch_policy_boundaries(hq, rows, cols, n_vec):
     """Each Q8_0 launch policy at and around its switch point (rows of at most
-    3072 columns at one vector; column-split stages at three or more vectors),
-    element by element against the oracle."""
+    3072 columns at one vector; column-split stages at three or more vectors,
+    with four or eight consumer warps), element by element against the oracle."""
     g = synthetic.rng(4242 + rows + cols + n_vec)
     blocks = quant("q8_0", synthetic.weights(g, rows, cols))
     x = synthetic.activations(g, n_vec, cols)

@@ -120,6 +120,26 @@ def test_plan_invariants(hq, fmt):
             assert 1 <= p["grid"] <= min(p["tiles"], p["slots"]), what
 
 
+@pytest.mark.parametrize("rows,cols,n_vec,warps", [
+    (1024, 3072, 8, 8),     # short rows, K split kept with eight warps
+    (4096, 1024, 4, 8),
+    (4096, 14336, 4, 8),    # four vectors, long rows
+    (4096, 14336, 8, 4),    # eight vectors on long rows: four warps
+    (6144, 4096, 4, 4),     # eight warps would halve the K split (2 instead of 4)
+    (28672, 4096, 4, 4),    # no K split
+    (128256, 4096, 8, 4),
+])
+def test_q8_0_wide_warps(hq, rows, cols, n_vec, warps):
+    """Q8_0 at three or more vectors takes eight consumer warps of one block
+    each only on K-split launches that keep their split with them, on rows of
+    at most 3072 columns or at four vectors or fewer; four warps otherwise."""
+    p = plan(hq, 8, n_vec, rows, cols, 100)
+    assert p["policy"] == 4 and p["tile_rows"] == 64
+    assert p["cons_warps"] == warps, p
+    if warps == 8:
+        assert p["ksplit"] > 1 and p["ctas_per_sm"] == 2
+
+
 def test_plan_rejects_bad_arguments(hq):
     with pytest.raises(hq.HQError):
         hq.hq_debug_plan(3, 1, 64, 256, 152, 232448, 80)        # no such format
