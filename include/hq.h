@@ -406,7 +406,7 @@ uint64_t hq_launch_count(void);
  *         128), the shapes the TMA-staged kernel serves.
  *   out : int64 [out_len >= HQ_PLAN_FIELDS], caller-owned host memory,
  *         filled with { policy (0 one owner per stage, 1 Q8_0 short rows,
- *         2 Q8_0 two vectors, 4 column-split stages; 3 is not used),
+ *         4 column-split stages; 2 and 3 are not used),
  *         consumer warps per CTA,
  *         rows per tile, grid (CTAs), K split (CTAs per cluster), ring stages,
  *         dynamic shared memory bytes, CTAs per SM of the launch bound,

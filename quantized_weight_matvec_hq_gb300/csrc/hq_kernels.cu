@@ -188,11 +188,6 @@ constexpr long long kShortRowCols = 3072;
 struct PolQ8_0Moe : PolQ8_0 {
     static constexpr int kConsWarpsFewAcc = 3;
 };
-// Q8_0 at two vectors: three consumer warps per CTA, with a ring of one
-// stage per warp (8B-shaped token 3714 -> 3819 GB/s).
-struct PolQ8_0Two : PolQ8_0 {
-    static constexpr int kConsWarpsFewAcc = 3;
-};
 
 // Q8_0 at three or more vectors: the block scale is folded into each weight,
 // so a lane carries several rows without per-block partial sums (their
@@ -1652,12 +1647,11 @@ Plan make_plan(const DeviceInfo &dev, long long n_work, int n_chunks, int regs_p
     // Q4_0 token: 3154 GB/s with three warps and two stages each, 3411 with
     // three warps and one, 3568 with four warps and one.  The MoE kernel at one
     // vector does the same with three warps (48-layer step 2399 -> 2526 GB/s),
-    // and so does the dense Q8_0 kernel at two vectors (PolQ8_0Two); the dense
+    // and so did the dense Q8_0 kernel at two vectors before its wide policy; the dense
     // Q8_0 kernel at one vector does not (8B token 5186 -> 4607 GB/s), nor the
     // MoE kernel at four vectors (2696 -> 2579 GB/s).
     constexpr int kSpw = (((P::kNibbles || std::is_same<P, PolQ8_0Moe>::value) && NV == 1) ||
-                          (P::kNibbles && NV == 2) ||
-                          (std::is_same<P, PolQ8_0Two>::value && NV == 2)) ? 1 : 2;
+                          (P::kNibbles && NV == 2)) ? 1 : 2;
     p.stages = SH ? 2 : kSpw * SQ;
     while (L::total(p.stages + SQ, 1) * want <= budget && p.stages < 4 * SQ) p.stages += SQ;
     p.smem = L::total(p.stages, 1);
@@ -1888,17 +1882,19 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
     constexpr int R = rows_per_lane<P>(NV);
     using RT = std::integral_constant<int, R>;
     if constexpr (std::is_same<P, PolQ8_0>::value && NV == 1) {
+        // (the wide policy below lost here: 8B-shaped token 4970 -> 4581 GB/s,
+        // and 4967 -> 4647 with it on the launches without a K split only,
+        // although gate|up alone gained 5182 -> 5548)
         if (cols <= kShortRowCols) return f(PolQ8_0Short{}, RT{});
         return f(P{}, RT{});
-    } else if constexpr (std::is_same<P, PolQ8_0>::value && NV == 2) {
-        return f(PolQ8_0Two{}, RT{});
     } else if constexpr (std::is_same<P, PolQ8_0>::value) {
-        // Q8_0 at three or more vectors: column-split stages of 64-row tiles, two
+        // Q8_0 at two or more vectors: column-split stages of 64-row tiles, two
         // rows per lane, the scale folded into each weight (PolQ8_0Wide).  Against
         // the row-split stages of one row per lane it replaced (one 32-row share
         // of every stage per warp), the 8B-shaped token at n_vec 3 / 4 / 5 / 8:
-        // 3280 / 2716 / 2045 / 1335 -> 3605 / 2952 / 2764 / 2135 GB/s.  Three
-        // rows per lane (96-row tiles) lost on the K-split launches.
+        // 3280 / 2716 / 2045 / 1335 -> 3605 / 2952 / 2764 / 2135 GB/s; at n_vec 2,
+        // against three warps each owning a stage of 32 rows, 3784 -> 4175.
+        // Three rows per lane (96-row tiles) lost on the K-split launches.
         // Eight consumer warps, one block each (PolQ8_0Wide8), on launches that
         // split K and keep the same split with them (the launch's CTAs then bring
         // twice the warps): rows of at most 3072 columns at every n_vec
@@ -1969,7 +1965,6 @@ hq_status dense_nv(const DeviceInfo &dev, const void *W, const void *x, void *y,
 template <class Pol>
 constexpr int policy_id() {
     return std::is_same<Pol, PolQ8_0Short>::value ? 1
-         : std::is_same<Pol, PolQ8_0Two>::value ? 2
          : Pol::kColSplit ? 4 : 0;
 }
 

@@ -453,6 +453,8 @@ def test_moe_invalid_id_sets_fault_and_nan(hq, flags):
     (97, 3328, 1),      # one K chunk past the short-row limit: two warps, K split over a cluster
     (1000, 1024, 1),    # short rows, many tiles
     (4100, 4096, 3),    # column-split stages (64-row tiles, two rows per lane), ragged last tile
+    (14593, 512, 2),    # two vectors: column-split stages without a K split, ragged last tile
+    (97, 3328, 2),      # two vectors, K split over a cluster
     (4100, 4096, 6),
     (333, 14336, 7),    # column-split stages with a K split over a cluster
     (4100, 4096, 3),    # eight consumer warps of one block each (K split kept), ragged last tile
@@ -462,7 +464,7 @@ def test_moe_invalid_id_sets_fault_and_nan(hq, flags):
 ])
 def test_q8_0_launch_policy_boundaries(hq, rows, cols, n_vec):
     """Each Q8_0 launch policy at and around its switch point (rows of at most
-    3072 columns at one vector; column-split stages at three or more vectors,
+    3072 columns at one vector; column-split stages at two or more vectors,
     with four or eight consumer warps), element by element against the oracle."""
     g = synthetic.rng(4242 + rows + cols + n_vec)
     blocks = quant("q8_0", synthetic.weights(g, rows, cols))

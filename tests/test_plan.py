@@ -73,10 +73,8 @@ def test_plan_matches_the_recorded_launches(hq, args, want):
 def expected_policy(fmt, n_vec, rows, cols):
     if fmt == 8 and n_vec == 1:
         return 1 if cols <= 3072 else 0
-    if fmt == 8 and n_vec == 2:
-        return 2
     if fmt == 8:
-        return 4                # column-split stages, two rows per lane
+        return 4                # n_vec >= 2: column-split stages, two rows per lane
     if fmt in (4, 75) and n_vec >= 4:
         return 4                # column-split stages, two rows per lane
     if (fmt in (4, 75) and n_vec == 1) or (fmt == 4 and n_vec == 2):
@@ -99,7 +97,7 @@ def test_plan_invariants(hq, fmt):
         what = f"fmt {fmt} {rows}x{cols} n_vec={n_vec}: {p}"
         n_chunks = cols // chunk
         assert p["policy"] == expected_policy(fmt, n_vec, rows, cols), what
-        rpl = 2 if (fmt in (4, 75) and n_vec != 3) or (fmt == 8 and n_vec >= 3) else 1
+        rpl = 2 if (fmt in (4, 75) and n_vec != 3) or (fmt == 8 and n_vec >= 2) else 1
         assert p["tile_rows"] == 32 * rpl, what
         assert p["tiles"] == math.ceil(rows / p["tile_rows"]), what
         # the ring: one owner per stage (a multiple of the consumer warps), or at
@@ -130,7 +128,7 @@ def test_plan_invariants(hq, fmt):
     (128256, 4096, 8, 4),
 ])
 def test_q8_0_wide_warps(hq, rows, cols, n_vec, warps):
-    """Q8_0 at three or more vectors takes eight consumer warps of one block
+    """Q8_0 at two or more vectors takes eight consumer warps of one block
     each only on K-split launches that keep their split with them, on rows of
     at most 3072 columns or at four vectors or fewer; four warps otherwise."""
     p = plan(hq, 8, n_vec, rows, cols, 100)

@@ -94,3 +94,34 @@ def test_noalloc_takes_no_device_memory(hq):
     assert free1 == free0
     assert torch.equal(y, ref)
     assert hq.hq_device_fault() == 0
+
+
+def test_noalloc_in_captured_graph(hq):
+    """After one eager call (the device's set-up), the allocation-free call is
+    captured in a CUDA graph; two replays with different x give the eager
+    call's bits on the same x."""
+    rows, cols, rank, n_vec = 1000, 4096, 16, 2
+    blocks, A, B, x, Wd, Ad, Bd, xd = make(rows, cols, rank, n_vec, 1400)
+    g = synthetic.rng(1401)
+    xs = [synthetic.activations(g, n_vec, cols) for _ in range(2)]
+    y = torch.empty((n_vec, rows), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+    eager = []
+    with torch.cuda.stream(s):
+        for xi in xs:
+            xd.copy_(torch.from_numpy(xi))
+            hq.hq_matvec_q8_0_lora_noalloc(Wd, xd, Ad, Bd, 0.5, rank, y, rows, cols, n_vec,
+                                          stream=s.cuda_stream)
+            eager.append(y.clone())
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        hq.hq_matvec_q8_0_lora_noalloc(Wd, xd, Ad, Bd, 0.5, rank, y, rows, cols, n_vec,
+                                      stream=torch.cuda.current_stream().cuda_stream)
+    for xi, ref in zip(xs, eager):
+        xd.copy_(torch.from_numpy(xi))
+        y.fill_(float("nan"))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, ref)
+    assert hq.hq_device_fault() == 0
