@@ -611,6 +611,99 @@ struct PolQ4_0Wide : PolQ4_0 {
     }
 };
 
+// Q4_0 at four and five vectors on K-split launches: eight consumer warps,
+// each one block of every stage (as PolQ8_0Wide8), with PolQ4_0Wide's decode.
+struct PolQ4_0Wide8 : PolQ4_0Wide {
+    static constexpr int kConsWarps = 8;
+    static constexpr int kConsWarpsFewAcc = 8;
+
+    // block 2p + H: words 4H .. 4H + 4 of the pair at byte 36p (block 0: d in
+    // word 0's low half, quant bytes 2..17; block 1: d in word 4's high half,
+    // quant bytes in words 5..8)
+    template <int NV, int R, int H>
+    __device__ __forceinline__ static void consume_half(const uint8_t *__restrict__ wt,
+                                                        const uint8_t *__restrict__ xt8, int lane, int p,
+                                                        Acc (&acc)[R][NV]) {
+        const float *xt = reinterpret_cast<const float *>(xt8) + 64 * p + 32 * H;
+        const uint32_t magic = opaque_magic();
+        uint32_t w[R][5];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint32_t *rp =
+                reinterpret_cast<const uint32_t *>(wt + (lane + 32 * r) * kChunkBytes + 36 * p) + 4 * H;
+#pragma unroll
+            for (int k = 0; k < 5; ++k) w[r][k] = rp[k];
+        }
+        float2 d8[R], c8[R], d12[R], c12[R], d16[R], c16[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const unsigned short hb = H ? (unsigned short)(w[r][0] >> 16) : (unsigned short)(w[r][0] & 0xffffu);
+            const float d = __half2float(__ushort_as_half(hb));
+            const float e8 = d * 0.00390625f, e12 = d * 0.000244140625f, e16 = d * 0.0000152587890625f;
+            d8[r] = make_float2(e8, e8);
+            d12[r] = make_float2(e12, e12);
+            d16[r] = make_float2(e16, e16);
+            const float k8 = -8390656.0f * e8, k12 = -8421376.0f * e12, k16 = -8912896.0f * e16;
+            c8[r] = make_float2(k8, k8);
+            c12[r] = make_float2(k12, k12);
+            c16[r] = make_float2(k16, k16);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            uint32_t gw[R], gb[R];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                gw[r] = H ? w[r][1 + k] : __funnelshift_r(w[r][k], w[r][k + 1], 16);
+                gb[r] = prmt(gw[r], 0u, 0x0300u);
+            }
+            {
+                float4 xv[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 4 * k);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float2 w01 = ffma2(make_float2(nib<0xF00u>(gb[r], magic), nib<0xF00u>(gw[r], magic)),
+                                             d8[r], c8[r]);
+                    const float2 w23 = ffma2(make_float2(nib<0xF0000u>(gw[r], magic), nib<0xF0000u>(gb[r], magic)),
+                                             d16[r], c16[r]);
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        acc[r][v] = ffma2(w01, make_float2(xv[v].x, xv[v].y), acc[r][v]);
+                        acc[r][v] = ffma2(w23, make_float2(xv[v].z, xv[v].w), acc[r][v]);
+                    }
+                }
+            }
+            {
+                float4 xv[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 16 + 4 * k);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+                    const float2 w01 = ffma2(make_float2(nib<0xF000u>(gb[r], magic), nib<0xF000u>(gw[r], magic)),
+                                             d12[r], c12[r]);
+                    const float2 w23 = ffma2(make_float2(nib<0xF000u>(gw[r] >> 8, magic),
+                                                         nib<0xF000u>(gw[r] >> 16, magic)),
+                                             d12[r], c12[r]);
+#pragma unroll
+                    for (int v = 0; v < NV; ++v) {
+                        acc[r][v] = ffma2(w01, make_float2(xv[v].x, xv[v].y), acc[r][v]);
+                        acc[r][v] = ffma2(w23, make_float2(xv[v].z, xv[v].w), acc[r][v]);
+                    }
+                }
+            }
+        }
+    }
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume_one(const uint8_t *__restrict__ wt,
+                                                       const uint8_t *__restrict__ xt8, int lane, int b,
+                                                       Acc (&acc)[R][NV]) {
+        if (b & 1) consume_half<NV, R, 1>(wt, xt8, lane, b >> 1, acc);
+        else consume_half<NV, R, 0>(wt, xt8, lane, b >> 1, acc);
+    }
+};
+
 // Q4_K ("One Native Stack ...", sections "The Unified Quant Core" and "Ported
 // Versus Novel": ggml's super-block of 256 weights in 144 B).  A 256-column
 // chunk of a row is exactly one super-block: 16-byte unit 0 holds fp16 d,
@@ -1073,7 +1166,7 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 template <class P, int NV, int R>
 constexpr int ctas_per_sm() {
     // Q8_0 at three or more vectors: 75-104 registers, three CTAs of four consumer warps
-    if constexpr (std::is_base_of<PolQ8_0Wide8, P>::value) return 2;
+    if constexpr (std::is_base_of<PolQ8_0Wide8, P>::value || std::is_base_of<PolQ4_0Wide8, P>::value) return 2;
     if constexpr (std::is_base_of<PolQ8_0Wide, P>::value || std::is_base_of<PolQ4_0Wide, P>::value ||
                   std::is_base_of<PolQ4_KWide, P>::value)
         return 3;
@@ -1913,7 +2006,18 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
     } else if constexpr (std::is_same<P, PolQ4_0>::value && NV >= 4) {
         // the 4-bit formats from four vectors on, where the FP32 pipe binds: as
         // Q8_0 above (Q4_0 token n_vec 4 / 6 / 8: 1658 / 1284 / 1008 -> 1681 /
-        // 1326 / 1131 GB/s; at n_vec 3 it lost, 1930 -> 1730)
+        // 1326 / 1131 GB/s; at n_vec 3 it lost, 1930 -> 1730, and at 2 as well).
+        // Eight warps of one block each on K-split launches that keep their
+        // split, as for Q8_0, at four and five vectors (token n_vec 4 1679 ->
+        // 1712 GB/s); from six vectors on their 96-register bound spills.
+        if constexpr (NV <= 5) {
+            const long long tiles = (rows + 63) / 64;
+            const int chunks = (int)(cols / PolQ4_0::kChunkCols);
+            const Plan p4 = make_plan<PolColSplit<PolQ4_0Wide>, NV, 2, false>(dev, tiles, chunks, 0);
+            const Plan p8 = make_plan<PolColSplit<PolQ4_0Wide8>, NV, 2, false>(dev, tiles, chunks, 0);
+            if (p4.ksplit > 1 && p8.ksplit >= p4.ksplit)
+                return f(PolColSplit<PolQ4_0Wide8>{}, std::integral_constant<int, 2>{});
+        }
         return f(PolColSplit<PolQ4_0Wide>{}, std::integral_constant<int, 2>{});
     } else if constexpr (std::is_same<P, PolQ4_K>::value && NV >= 4) {
         // (Q4_K token n_vec 4 / 6 / 8: 1521 / 1192 / 953 -> 1569 / 1247 / 1075
