@@ -2023,13 +2023,14 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
         // (Q4_K token n_vec 4 / 6 / 8: 1521 / 1192 / 953 -> 1569 / 1247 / 1075
         // GB/s; at n_vec 3 it lost, 1752 -> 1682)
         return f(PolColSplit<PolQ4_KWide>{}, std::integral_constant<int, 2>{});
-    } else if constexpr (P::kNibbles && (NV == 1 || (NV == 2 && std::is_same<P, PolQ4_0>::value))) {
+    } else if constexpr (P::kNibbles && NV <= 2) {
         // column-split stages where the launch does not split K over clusters
         // (enough 64-row tiles to give every CTA slot two): Q4_0 gate|up
         // 28672x4096 3386 -> 3635 GB/s; with a K split they lost (o 4096x4096
         // 1622 -> 1482, down 4096x14336 2877 -> 2413 GB/s).  At two vectors
         // the Q4_0 token gained (2137 -> 2277 GB/s) and the Q4_K token lost
-        // (1995 -> 1885), whose decode holds more registers per row.  With the
+        // (1995 -> 1885), whose decode holds more registers per row; with the
+        // run-time pair offset below Q4_K gained too (2000 -> 2030).  With the
         // run-time pair offset below, column split on the K-split launches
         // still lost (Q4_0 token 3157 -> 2715, Q4_K 2572 -> 2397, Q4_0 at
         // two vectors 2398 -> 2289).

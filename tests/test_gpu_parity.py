@@ -480,8 +480,8 @@ def test_q8_0_launch_policy_boundaries(hq, rows, cols, n_vec):
     # column-split stages from 229 tiles on (ragged last tiles both sides)
     ("q4_0", 14592, 512, 1), ("q4_0", 14593, 512, 1), ("q4_0", 20000, 768, 1),
     ("q4_k", 14592, 512, 1), ("q4_k", 14593, 512, 1),
-    # Q4_0 at two vectors: column-split stages too (Q4_K keeps one stage per warp there)
-    ("q4_0", 14592, 512, 2), ("q4_0", 14593, 512, 2), ("q4_k", 14593, 512, 2),
+    # two vectors: column-split stages without a K split too
+    ("q4_0", 14592, 512, 2), ("q4_0", 14593, 512, 2), ("q4_k", 14592, 512, 2), ("q4_k", 14593, 512, 2),
     # four and five vectors: two rows per lane, eight warps on K-split launches
     ("q4_0", 300, 14336, 4), ("q4_0", 1000, 2048, 5), ("q4_0", 4100, 4096, 6), ("q4_k", 333, 14336, 4)])
 def test_nibble_launch_policy_boundaries(hq, fmt, rows, cols, n_vec):

@@ -77,7 +77,7 @@ def expected_policy(fmt, n_vec, rows, cols):
         return 4                # n_vec >= 2: column-split stages, two rows per lane
     if fmt in (4, 75) and n_vec >= 4:
         return 4                # column-split stages, two rows per lane
-    if (fmt in (4, 75) and n_vec == 1) or (fmt == 4 and n_vec == 2):
+    if fmt in (4, 75) and n_vec <= 2:
         # column-split stages unless K is split over clusters (64-row tiles too
         # few to give each of the 152 x 3 CTA slots two)
         return 4 if math.ceil(rows / 64) * 2 > GB300["num_sms"] * 3 else 0
