@@ -1977,7 +1977,9 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
     if constexpr (std::is_same<P, PolQ8_0>::value && NV == 1) {
         // (the wide policy below lost here: 8B-shaped token 4970 -> 4581 GB/s,
         // and 4967 -> 4647 with it on the launches without a K split only,
-        // although gate|up alone gained 5182 -> 5548)
+        // although gate|up alone gained 5182 -> 5548: its four-stage ring
+        // leaves the next launch no room; with three or two stages gate|up
+        // itself fell to 4825 / 4056 GB/s)
         if (cols <= kShortRowCols) return f(PolQ8_0Short{}, RT{});
         return f(P{}, RT{});
     } else if constexpr (std::is_same<P, PolQ8_0>::value) {
