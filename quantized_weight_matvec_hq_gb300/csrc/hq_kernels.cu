@@ -2008,7 +2008,9 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
     } else if constexpr (std::is_same<P, PolQ4_0>::value && NV >= 4) {
         // the 4-bit formats from four vectors on, where the FP32 pipe binds: as
         // Q8_0 above (Q4_0 token n_vec 4 / 6 / 8: 1658 / 1284 / 1008 -> 1681 /
-        // 1326 / 1131 GB/s; at n_vec 3 it lost, 1930 -> 1730, and at 2 as well).
+        // 1326 / 1131 GB/s; at n_vec 3 it lost, 1930 -> 1730, and at 2 as well;
+        // at 3 on the launches without a K split only, Q4_0 1928 -> 1852 and
+        // Q4_K 1743 -> 1701).
         // Eight warps of one block each on K-split launches that keep their
         // split, as for Q8_0, at four and five vectors (token n_vec 4 1679 ->
         // 1712 GB/s); from six vectors on their 96-register bound spills.
