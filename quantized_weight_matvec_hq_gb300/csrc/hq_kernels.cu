@@ -1,6 +1,6 @@
 // hq_kernels.cu -- the quantized-weight matvec kernels for sm_103a:
-// Q8_0 and Q4_0 float matvecs, their MoE (expert-indexed) variant, and the
-// per-output-channel int8 GEMV with gemmlowp requant.
+// Q8_0, Q4_0 and Q4_K float matvecs, the Q8_0 MoE (expert-indexed) variant,
+// and the per-output-channel int8 GEMV with gemmlowp requant.
 //
 // What is computed:
 //  * float formats ("One Native Stack for Private, Continuously-Learning AI",
@@ -30,7 +30,13 @@
 //  * int8 / nibble -> fp32 without conversion instructions: the byte goes
 //    into the mantissa of 2^23 (prmt), and 2^23 + bias is subtracted exactly
 //    with a packed fp32x2 add; products are packed fp32x2 FMAs.  The block sum
-//    is scaled by the block's fp16 d once per block.
+//    is scaled by the block's fp16 d once per block -- or, at two or more
+//    vectors, d is folded into each weight by one exact packed fma (q d is
+//    formed before it multiplies x), which frees the per-block sums'
+//    registers for a second row per lane.
+//  * Column-split stages: all consumer warps work on every stage, each on its
+//    own blocks, decoded at a run-time offset so that one copy of the
+//    unrolled decode serves every warp.
 //  * Matrices with few row tiles split K over a thread-block cluster; the
 //    partial sums are combined through distributed shared memory in a fixed
 //    order (no atomics, so results are deterministic).  Large matrices run
