@@ -299,10 +299,11 @@ def test_full_size_lm_heads_sampled(hq, fmt, rows, cols):
                                               synthetic.QWEN3_0_6B_LAYER + synthetic.fuse_same_input(synthetic.QWEN3_0_6B_LAYER)}))
 def test_qwen3_0_6b_layer_shapes_full(hq, rows, cols):
     """Every Qwen3-0.6B-shaped decode matvec (unfused and with q|k|v, gate|up
-    row-fused), Q8_0, every output checked, n_vec 1 and 2."""
+    row-fused), Q8_0, every output checked, n_vec 1, 2, 4 and 8 (the short-row
+    K-split launches take eight consumer warps from two vectors on)."""
     g = synthetic.rng(synthetic.SEED_BASE + 1)
     blocks = quant("q8_0", synthetic.weights(g, rows, cols))
-    for n_vec in (1, 2):
+    for n_vec in (1, 2, 4, 8):
         x = synthetic.activations(g, n_vec, cols)
         y_ref, T = oracle.matvec("q8_0", blocks, x, rows, cols)
         y = gpu_matvec(hq, "q8_0", blocks, x, rows, cols)

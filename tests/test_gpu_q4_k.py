@@ -131,7 +131,7 @@ def test_x_magnitudes(hq, scale):
     rows, cols = 128, 1024
     g = synthetic.rng(1200)
     blocks = oracle.quantize_q4_k(synthetic.weights(g, rows, cols))
-    for n_vec in (1, 3):
+    for n_vec in (1, 3, 5, 8):
         x = (synthetic.activations(g, n_vec, cols).astype(np.float64) * scale).astype(np.float32)
         y_ref, T = oracle.matvec("q4_k", blocks, x, rows, cols)
         assert_within(gpu_q4_k(hq, blocks, x, rows, cols), y_ref, T, f"x scale {scale} n_vec={n_vec}")
