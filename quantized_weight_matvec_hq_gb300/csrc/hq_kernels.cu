@@ -918,6 +918,74 @@ struct PolQ4_KWide : PolQ4_K {
     }
 };
 
+// Q4_K at four vectors on K-split launches: eight consumer warps,
+// warp b one sub-block of every stage (the low nibbles of quant group b / 2
+// for even b, the high nibbles for odd b), as PolQ8_0Wide8 does for Q8_0.
+struct PolQ4_KWide8 : PolQ4_KWide {
+    static constexpr int kConsWarps = 8;
+    static constexpr int kConsWarpsFewAcc = 8;
+
+    template <int NV, int R, int HI>
+    __device__ __forceinline__ static void consume_sub(const uint8_t *__restrict__ wt,
+                                                       const uint8_t *__restrict__ xt8, int lane, int p,
+                                                       Acc (&acc)[R][NV]) {
+        const float *xt = reinterpret_cast<const float *>(xt8) + 64 * p + 32 * HI;
+        const float2 kM = make_float2(-8388608.0f, -8388608.0f);          // -2^23
+        const uint32_t magic = opaque_magic();
+        float2 aa[R], bb[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const uint4 hdr = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes)[0];
+            const float d = __half2float(__ushort_as_half((unsigned short)(hdr.x & 0xffffu)));
+            const float dm = __half2float(__ushort_as_half((unsigned short)(hdr.x >> 16)));
+            const float a = d * (float)six_rt(2 * p + HI, 0, hdr.y, hdr.z, hdr.w);
+            const float b = dm * (float)six_rt(2 * p + HI, 1, hdr.y, hdr.z, hdr.w);
+            aa[r] = HI ? make_float2(a * 0.0625f, a * 0.000244140625f)      // nibbles at bits 4 and 12
+                       : make_float2(a, a * 0.00390625f);                  // nibbles at bits 0 and 8
+            bb[r] = make_float2(-b, -b);
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            uint32_t qw[R][4];
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                const uint4 q = reinterpret_cast<const uint4 *>(wt + (lane + 32 * r) * kChunkBytes)[1 + 2 * p + u];
+                qw[r][0] = q.x; qw[r][1] = q.y; qw[r][2] = q.z; qw[r][3] = q.w;
+            }
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const int k = 4 * u + kk;
+                float4 xv[NV];
+#pragma unroll
+                for (int v = 0; v < NV; ++v)
+                    xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 4 * k);
+#pragma unroll
+                for (int r = 0; r < R; ++r) {
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t w = h ? (qw[r][kk] >> 16) : qw[r][kk];
+                        const float2 q = HI ? fadd2(make_float2(nib<0xF0u>(w, magic), nib<0xF000u>(w, magic)), kM)
+                                            : fadd2(make_float2(nib<0xFu>(w, magic), nib<0xF00u>(w, magic)), kM);
+                        const float2 wq = ffma2(aa[r], q, bb[r]);
+#pragma unroll
+                        for (int v = 0; v < NV; ++v) {
+                            const float2 xp = h ? make_float2(xv[v].z, xv[v].w) : make_float2(xv[v].x, xv[v].y);
+                            acc[r][v] = ffma2(wq, xp, acc[r][v]);
+                        }
+                    }
+                }
+            }
+        }
+    }
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume_one(const uint8_t *__restrict__ wt,
+                                                       const uint8_t *__restrict__ xt8, int lane, int b,
+                                                       Acc (&acc)[R][NV]) {
+        if (b & 1) consume_sub<NV, R, 1>(wt, xt8, lane, b >> 1, acc);
+        else consume_sub<NV, R, 0>(wt, xt8, lane, b >> 1, acc);
+    }
+};
+
 struct PolI8 {
     static constexpr int kChunkCols = 128;          // one 128-byte swizzle span
     static constexpr int kChunkBytes = 128;
@@ -1172,7 +1240,9 @@ __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("grid
 template <class P, int NV, int R>
 constexpr int ctas_per_sm() {
     // Q8_0 at three or more vectors: 75-104 registers, three CTAs of four consumer warps
-    if constexpr (std::is_base_of<PolQ8_0Wide8, P>::value || std::is_base_of<PolQ4_0Wide8, P>::value) return 2;
+    if constexpr (std::is_base_of<PolQ8_0Wide8, P>::value || std::is_base_of<PolQ4_0Wide8, P>::value ||
+                  std::is_base_of<PolQ4_KWide8, P>::value)
+        return 2;
     if constexpr (std::is_base_of<PolQ8_0Wide, P>::value || std::is_base_of<PolQ4_0Wide, P>::value ||
                   std::is_base_of<PolQ4_KWide, P>::value)
         return 3;
@@ -2030,6 +2100,17 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
         }
         return f(PolColSplit<PolQ4_0Wide>{}, std::integral_constant<int, 2>{});
     } else if constexpr (std::is_same<P, PolQ4_K>::value && NV >= 4) {
+        // eight warps of one sub-block each on K-split launches that keep their
+        // split, at four vectors (token 1566 -> 1579 GB/s; at five their
+        // 96-register bound spills)
+        if constexpr (NV == 4) {
+            const long long tiles = (rows + 63) / 64;
+            const int chunks = (int)(cols / PolQ4_K::kChunkCols);
+            const Plan p4 = make_plan<PolColSplit<PolQ4_KWide>, NV, 2, false>(dev, tiles, chunks, 0);
+            const Plan p8 = make_plan<PolColSplit<PolQ4_KWide8>, NV, 2, false>(dev, tiles, chunks, 0);
+            if (p4.ksplit > 1 && p8.ksplit >= p4.ksplit)
+                return f(PolColSplit<PolQ4_KWide8>{}, std::integral_constant<int, 2>{});
+        }
         // (Q4_K token n_vec 4 / 6 / 8: 1521 / 1192 / 953 -> 1569 / 1247 / 1075
         // GB/s; at n_vec 3 it lost, 1752 -> 1682)
         return f(PolColSplit<PolQ4_KWide>{}, std::integral_constant<int, 2>{});

@@ -149,6 +149,17 @@ def test_q4_0_wide_warps(hq, rows, cols, n_vec, warps):
     assert p["cons_warps"] == warps, p
 
 
+@pytest.mark.parametrize("rows,cols,n_vec,warps", [
+    (4096, 14336, 4, 8), (4096, 14336, 5, 4), (28672, 4096, 4, 4),
+])
+def test_q4_k_wide_warps(hq, rows, cols, n_vec, warps):
+    """Q4_K takes eight warps on K-split launches that keep their split at four
+    vectors only."""
+    p = plan(hq, 75, n_vec, rows, cols, 100)
+    assert p["policy"] == 4 and p["tile_rows"] == 64
+    assert p["cons_warps"] == warps, p
+
+
 def test_plan_rejects_bad_arguments(hq):
     with pytest.raises(hq.HQError):
         hq.hq_debug_plan(3, 1, 64, 256, 152, 232448, 80)        # no such format
