@@ -2055,7 +2055,8 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
         // and 4967 -> 4647 with it on the launches without a K split only,
         // although gate|up alone gained 5182 -> 5548: its four-stage ring
         // leaves the next launch no room; with three or two stages gate|up
-        // itself fell to 4825 / 4056 GB/s)
+        // itself fell to 4825 / 4056 GB/s; eight warps on the short-row K-split
+        // launches alone lost too, Qwen3-0.6B token 1609 -> 1448 GB/s)
         if (cols <= kShortRowCols) return f(PolQ8_0Short{}, RT{});
         return f(P{}, RT{});
     } else if constexpr (std::is_same<P, PolQ8_0>::value) {
