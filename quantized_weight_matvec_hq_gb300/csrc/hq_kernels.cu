@@ -215,69 +215,6 @@ struct PolQ8_0Wide : PolQ8_0 {
     static constexpr bool kComputeBound = true;     // the FP32 pipe, not HBM, sets the pace at eight vectors
     static constexpr bool kRuntimeCols = true;      // see consume_pair
 
-    // Blocks 2p and 2p + 1 of the stage's chunk for R rows per lane.  The pair
-    // is 68 bytes from byte 68p of each row chunk: 17 words from a 4-byte
-    // aligned start, the same word and byte positions for every p.  So p is a
-    // run-time value and one copy of this code serves all four warps of a
-    // column split (four copies with constant offsets overflow the SM's
-    // instruction cache at these unroll depths).
-    template <int NV, int R>
-    __device__ __forceinline__ static void consume_pair(const uint8_t *__restrict__ wt,
-                                                        const uint8_t *__restrict__ xt8, int lane, int p,
-                                                        Acc (&acc)[R][NV]) {
-        const float *xt = reinterpret_cast<const float *>(xt8) + 64 * p;
-        uint32_t w[R][17];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint32_t *rp = reinterpret_cast<const uint32_t *>(wt + (lane + 32 * r) * kChunkBytes + 68 * p);
-#pragma unroll
-            for (int k = 0; k < 17; ++k) w[r][k] = rp[k] ^ 0x80808080u;   // quant bytes q + 128 (and d's bytes flipped)
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float2 dd[R], cc[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const unsigned short hb = (unsigned short)((h ? (w[r][8] >> 16) : (w[r][0] & 0xffffu)) ^ 0x8080u);
-                const float dq = __half2float(__ushort_as_half(hb)) * 0.00390625f;   // d / 256, exact
-                const float c = -8421376.0f * dq;                                   // -(2^23 + 2^15) d / 256, exact
-                dd[r] = make_float2(dq, dq);
-                cc[r] = make_float2(c, c);
-            }
-#pragma unroll
-            for (int g = 0; g < 8; ++g) {
-                float4 xv[NV];
-#pragma unroll
-                for (int v = 0; v < NV; ++v)
-                    xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * h + 4 * g);
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    float f[4];
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int o = 34 * h + 2 + 4 * g + i;     // byte of quant 4g+i in the pair
-                        f[i] = byte_mid_as_float(w[r][o >> 2], o & 3);
-                    }
-                    const float2 w01 = ffma2(make_float2(f[0], f[1]), dd[r], cc[r]);
-                    const float2 w23 = ffma2(make_float2(f[2], f[3]), dd[r], cc[r]);
-#pragma unroll
-                    for (int v = 0; v < NV; ++v) {
-                        acc[r][v] = ffma2(w01, make_float2(xv[v].x, xv[v].y), acc[r][v]);
-                        acc[r][v] = ffma2(w23, make_float2(xv[v].z, xv[v].w), acc[r][v]);
-                    }
-                }
-            }
-        }
-    }
-};
-
-// Q8_0 at three or more vectors on launches that split K over clusters: eight
-// consumer warps, each one block of every stage, so that the launch's few CTAs
-// (1.7 per SM on the 8B-shaped o, q|k|v and down) bring twice the warps.
-struct PolQ8_0Wide8 : PolQ8_0Wide {
-    static constexpr int kConsWarps = 8;
-    static constexpr int kConsWarpsFewAcc = 8;
-
     // block 2p + H of the chunk: words 8H .. 8H + 8 of the pair at byte 68p
     // (block 0: d in word 0's low half, quant bytes 2..33; block 1: d in word
     // 8's high half, quant bytes in words 9..16)
@@ -327,6 +264,28 @@ struct PolQ8_0Wide8 : PolQ8_0Wide {
             }
         }
     }
+    // Blocks 2p and 2p + 1 of the stage's chunk for R rows per lane.  The pair
+    // is 68 bytes from byte 68p of each row chunk: 17 words from a 4-byte
+    // aligned start, the same word and byte positions for every p.  So p is a
+    // run-time value and one copy of this code serves all four warps of a
+    // column split (four copies with constant offsets overflow the SM's
+    // instruction cache at these unroll depths).
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume_pair(const uint8_t *__restrict__ wt,
+                                                        const uint8_t *__restrict__ xt8, int lane, int p,
+                                                        Acc (&acc)[R][NV]) {
+        consume_half<NV, R, 0>(wt, xt8, lane, p, acc);
+        consume_half<NV, R, 1>(wt, xt8, lane, p, acc);
+    }
+};
+
+// Q8_0 at three or more vectors on launches that split K over clusters: eight
+// consumer warps, each one block of every stage, so that the launch's few CTAs
+// (1.7 per SM on the 8B-shaped o, q|k|v and down) bring twice the warps.
+struct PolQ8_0Wide8 : PolQ8_0Wide {
+    static constexpr int kConsWarps = 8;
+    static constexpr int kConsWarpsFewAcc = 8;
+
     template <int NV, int R>
     __device__ __forceinline__ static void consume_one(const uint8_t *__restrict__ wt,
                                                        const uint8_t *__restrict__ xt8, int lane, int b,
@@ -532,97 +491,6 @@ struct PolQ4_0Pair : PolQ4_0 {
 struct PolQ4_0Wide : PolQ4_0 {
     static constexpr bool kRuntimeCols = true;      // see consume_pair
 
-    // Blocks 2p and 2p + 1 of the stage's chunk: 36 bytes from byte 36p of each
-    // row chunk, 9 words from a 4-byte-aligned start (block 0: d in word 0's
-    // low half, quant bytes from byte 2; block 1: d in word 4's high half,
-    // quant bytes in words 5..8).
-    template <int NV, int R>
-    __device__ __forceinline__ static void consume_pair(const uint8_t *__restrict__ wt,
-                                                        const uint8_t *__restrict__ xt8, int lane, int p,
-                                                        Acc (&acc)[R][NV]) {
-        const float *xt = reinterpret_cast<const float *>(xt8) + 64 * p;
-        const uint32_t magic = opaque_magic();
-        uint32_t w[R][9];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            const uint32_t *rp = reinterpret_cast<const uint32_t *>(wt + (lane + 32 * r) * kChunkBytes + 36 * p);
-#pragma unroll
-            for (int k = 0; k < 9; ++k) w[r][k] = rp[k];
-        }
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            float2 d8[R], c8[R], d12[R], c12[R], d16[R], c16[R];
-#pragma unroll
-            for (int r = 0; r < R; ++r) {
-                const unsigned short hb = h ? (unsigned short)(w[r][4] >> 16) : (unsigned short)(w[r][0] & 0xffffu);
-                const float d = __half2float(__ushort_as_half(hb));
-                const float e8 = d * 0.00390625f, e12 = d * 0.000244140625f, e16 = d * 0.0000152587890625f;
-                d8[r] = make_float2(e8, e8);
-                d12[r] = make_float2(e12, e12);
-                d16[r] = make_float2(e16, e16);
-                const float k8 = -8390656.0f * e8, k12 = -8421376.0f * e12, k16 = -8912896.0f * e16;
-                c8[r] = make_float2(k8, k8);        // -(2^23 + 2^11) d / 2^8
-                c12[r] = make_float2(k12, k12);     // -(2^23 + 2^15) d / 2^12
-                c16[r] = make_float2(k16, k16);     // -(2^23 + 2^19) d / 2^16
-            }
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                // quant bytes 4k..4k+3 of block h: low nibbles are q_{4k..4k+3},
-                // high nibbles q_{16+4k..16+4k+3}
-                uint32_t gw[R], gb[R];
-#pragma unroll
-                for (int r = 0; r < R; ++r) {
-                    gw[r] = h ? w[r][5 + k] : __funnelshift_r(w[r][k], w[r][k + 1], 16);
-                    gb[r] = prmt(gw[r], 0u, 0x0300u);      // byte 0 at bits 8..15, byte 3 at 16..23
-                }
-                {
-                    float4 xv[NV];
-#pragma unroll
-                    for (int v = 0; v < NV; ++v)
-                        xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * h + 4 * k);
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const float2 w01 = ffma2(make_float2(nib<0xF00u>(gb[r], magic), nib<0xF00u>(gw[r], magic)),
-                                                 d8[r], c8[r]);
-                        const float2 w23 = ffma2(make_float2(nib<0xF0000u>(gw[r], magic), nib<0xF0000u>(gb[r], magic)),
-                                                 d16[r], c16[r]);
-#pragma unroll
-                        for (int v = 0; v < NV; ++v) {
-                            acc[r][v] = ffma2(w01, make_float2(xv[v].x, xv[v].y), acc[r][v]);
-                            acc[r][v] = ffma2(w23, make_float2(xv[v].z, xv[v].w), acc[r][v]);
-                        }
-                    }
-                }
-                {
-                    float4 xv[NV];
-#pragma unroll
-                    for (int v = 0; v < NV; ++v)
-                        xv[v] = *reinterpret_cast<const float4 *>(xt + v * kChunkCols + 32 * h + 16 + 4 * k);
-#pragma unroll
-                    for (int r = 0; r < R; ++r) {
-                        const float2 w01 = ffma2(make_float2(nib<0xF000u>(gb[r], magic), nib<0xF000u>(gw[r], magic)),
-                                                 d12[r], c12[r]);
-                        const float2 w23 = ffma2(make_float2(nib<0xF000u>(gw[r] >> 8, magic),
-                                                             nib<0xF000u>(gw[r] >> 16, magic)),
-                                                 d12[r], c12[r]);
-#pragma unroll
-                        for (int v = 0; v < NV; ++v) {
-                            acc[r][v] = ffma2(w01, make_float2(xv[v].x, xv[v].y), acc[r][v]);
-                            acc[r][v] = ffma2(w23, make_float2(xv[v].z, xv[v].w), acc[r][v]);
-                        }
-                    }
-                }
-            }
-        }
-    }
-};
-
-// Q4_0 at four and five vectors on K-split launches: eight consumer warps,
-// each one block of every stage (as PolQ8_0Wide8), with PolQ4_0Wide's decode.
-struct PolQ4_0Wide8 : PolQ4_0Wide {
-    static constexpr int kConsWarps = 8;
-    static constexpr int kConsWarpsFewAcc = 8;
-
     // block 2p + H: words 4H .. 4H + 4 of the pair at byte 36p (block 0: d in
     // word 0's low half, quant bytes 2..17; block 1: d in word 4's high half,
     // quant bytes in words 5..8)
@@ -701,6 +569,24 @@ struct PolQ4_0Wide8 : PolQ4_0Wide {
             }
         }
     }
+    // Blocks 2p and 2p + 1 of the stage's chunk: 36 bytes from byte 36p of each
+    // row chunk, 9 words from a 4-byte-aligned start, the same positions for
+    // every p, so p is a run-time value.
+    template <int NV, int R>
+    __device__ __forceinline__ static void consume_pair(const uint8_t *__restrict__ wt,
+                                                        const uint8_t *__restrict__ xt8, int lane, int p,
+                                                        Acc (&acc)[R][NV]) {
+        consume_half<NV, R, 0>(wt, xt8, lane, p, acc);
+        consume_half<NV, R, 1>(wt, xt8, lane, p, acc);
+    }
+};
+
+// Q4_0 at four and five vectors on K-split launches: eight consumer warps,
+// each one block of every stage (as PolQ8_0Wide8), with PolQ4_0Wide's decode.
+struct PolQ4_0Wide8 : PolQ4_0Wide {
+    static constexpr int kConsWarps = 8;
+    static constexpr int kConsWarpsFewAcc = 8;
+
     template <int NV, int R>
     __device__ __forceinline__ static void consume_one(const uint8_t *__restrict__ wt,
                                                        const uint8_t *__restrict__ xt8, int lane, int b,
