@@ -581,7 +581,7 @@ struct PolQ4_0Wide : PolQ4_0 {
     }
 };
 
-// Q4_0 at four and five vectors on K-split launches: eight consumer warps,
+// Q4_0 at three to five vectors on K-split launches: eight consumer warps,
 // each one block of every stage (as PolQ8_0Wide8), with PolQ4_0Wide's decode.
 struct PolQ4_0Wide8 : PolQ4_0Wide {
     static constexpr int kConsWarps = 8;
@@ -804,7 +804,7 @@ struct PolQ4_KWide : PolQ4_K {
     }
 };
 
-// Q4_K at four vectors on K-split launches: eight consumer warps,
+// Q4_K at three and four vectors on K-split launches: eight consumer warps,
 // warp b one sub-block of every stage (the low nibbles of quant group b / 2
 // for even b, the high nibbles for odd b), as PolQ8_0Wide8 does for Q8_0.
 struct PolQ4_KWide8 : PolQ4_KWide {
@@ -1968,6 +1968,26 @@ hq_status with_dense_policy(const DeviceInfo &dev, long long rows, long long col
                 return f(PolColSplit<PolQ8_0Wide8>{}, std::integral_constant<int, 2>{});
         }
         return f(PolColSplit<PolQ8_0Wide>{}, std::integral_constant<int, 2>{});
+    } else if constexpr (P::kNibbles && NV == 3) {
+        // three vectors: one owner per stage and one row per lane, except on
+        // K-split launches that keep their split with eight warps of one block
+        // each (Q4_0 token 1931 -> 1959 GB/s; the four-warp wide layout lost
+        // here, see below)
+        const long long tiles = (rows + 63) / 64;
+        const int chunks = (int)(cols / P::kChunkCols);
+        if constexpr (std::is_same<P, PolQ4_0>::value) {
+            const Plan p4 = make_plan<PolColSplit<PolQ4_0Wide>, NV, 2, false>(dev, tiles, chunks, 0);
+            const Plan p8 = make_plan<PolColSplit<PolQ4_0Wide8>, NV, 2, false>(dev, tiles, chunks, 0);
+            if (p4.ksplit > 1 && p8.ksplit >= p4.ksplit)
+                return f(PolColSplit<PolQ4_0Wide8>{}, std::integral_constant<int, 2>{});
+        } else {
+            // (Q4_K token 1742 -> 1761 GB/s)
+            const Plan p4 = make_plan<PolColSplit<PolQ4_KWide>, NV, 2, false>(dev, tiles, chunks, 0);
+            const Plan p8 = make_plan<PolColSplit<PolQ4_KWide8>, NV, 2, false>(dev, tiles, chunks, 0);
+            if (p4.ksplit > 1 && p8.ksplit >= p4.ksplit)
+                return f(PolColSplit<PolQ4_KWide8>{}, std::integral_constant<int, 2>{});
+        }
+        return f(P{}, RT{});
     } else if constexpr (std::is_same<P, PolQ4_0>::value && NV >= 4) {
         // the 4-bit formats from four vectors on, where the FP32 pipe binds: as
         // Q8_0 above (Q4_0 token n_vec 4 / 6 / 8: 1658 / 1284 / 1008 -> 1681 /
